@@ -1,0 +1,205 @@
+/*
+ * msa.h -- C ABI of libmsa.so: Multi-Segment Attention (MSA) on one B300 (sm_103a).
+ *
+ * Source: "Multi-Segment Attention: Enabling Efficient KV-Cache Management for
+ * Faster Large Language Model Serving" (Shi, Chen, Chen, Miao, Cui), abstract,
+ * Fig. 1 / Eq. 1 (attention), Fig. 4 / section 4.1 (non-contiguous cache segments
+ * are disjoint KV regions), Fig. 5 (MSA).
+ *
+ * What MSA computes.  A query chunk -- recomputed evicted KV blocks plus new tokens,
+ * each at its ORIGINAL position -- attends exactly (Eq. 1, scale 1/sqrt(d)) over a
+ * KV context that is the union of many non-contiguous segments: cached paged blocks
+ * plus the chunk's own freshly computed K/V, with a causal mask by original position
+ * (key position <= query position, the query itself included).  Query head h reads
+ * KV head h / (Hq/Hkv).  Outputs are O (bf16) and LSE = ln(sum_j exp(scale*q.k_j))
+ * (fp32, natural log).  Decode: the newest token of each sequence (its own K/V
+ * already in the pool) attends over every KV token of its sequence.
+ *
+ * Conventions.
+ *  - All tensors named "device" are device pointers owned by the caller.  The
+ *    library never allocates device memory.  The library owns only the opaque host
+ *    plan object.
+ *  - Launch functions are asynchronous on the given stream; they return argument and
+ *    launch errors at once.  Errors found on the device (a bounded wait that ran out)
+ *    are written to the workspace status word and read by msa_get_status.
+ *  - bf16 tensors are raw IEEE bfloat16 (uint16) arrays, row-major, densely packed.
+ *  - All validation of the layout happens in msa_plan_create.
+ *  - Plans are immutable after creation and may be used from several threads.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = -1,   /* null pointer, bad count, unsorted q_pos, inconsistent run */
+  MSA_ERR_UNSUPPORTED = -2,   /* head_dim not in {64,128}, block_size != 16, Hq % Hkv != 0 */
+  MSA_ERR_POS_OVERLAP = -3,   /* two KV tokens of one sequence share an original position */
+  MSA_ERR_BLOCK_OOB = -4,     /* block id outside [0, num_pool_blocks) or logical block outside the row */
+  MSA_ERR_WORKSPACE = -5,     /* workspace or output buffer too small / misaligned */
+  MSA_ERR_CUDA = -6,          /* a CUDA runtime call failed (launch, copy, tensor map) */
+  MSA_ERR_TIMEOUT = -7,       /* a device wait ran past its bound; the kernel gave up */
+  MSA_ERR_MODE = -8           /* plan built for the other mode */
+} msa_status_t;
+
+typedef enum { MSA_PREFILL = 0, MSA_DECODE = 1 } msa_mode_t;
+
+/* One segment: a run of `num_blocks` logical blocks of row `seq` of the block table,
+ * starting at logical block `first_logical_block`, whose original positions are
+ * consecutive: block_pos[bt[k+1]] == block_pos[bt[k]] + 16, and only the last block
+ * of a run may hold fewer than 16 tokens (section 4.1: a cache segment is one
+ * disjoint KV region; the paged block layout follows the paged KV cache the paper
+ * builds on). */
+typedef struct {
+  int32_t seq;
+  int32_t first_logical_block;
+  int32_t num_blocks;
+} msa_segment_t;
+
+typedef struct {
+  int32_t num_heads_q;        /* Hq */
+  int32_t num_heads_kv;       /* Hkv, Hq % Hkv == 0 */
+  int32_t head_dim;           /* d, 64 or 128 */
+  int32_t block_size;         /* tokens per pool block, must be 16 */
+  int32_t decode_split_blocks;/* decode: pool blocks per split-KV work unit, 0 = automatic */
+  int32_t decode_min_ctas;    /* decode: target number of CTAs when automatic, 0 = 16 x SMs */
+  int32_t reserved[4];        /* must be 0 */
+} msa_plan_opts_t;
+
+typedef struct msa_plan msa_plan_t;
+
+typedef struct {
+  int64_t useful_flops;       /* 4 * d * Hq * number of visible (query, key) pairs */
+  int64_t kv_tokens;          /* KV tokens over all sequences (pool + chunk) */
+  int64_t algorithmic_bytes;  /* decode: K/V + Q + O + LSE + block metadata bytes read/written once */
+  int32_t num_kv_tiles;
+  int32_t num_q_tiles;
+  int32_t num_work_items;     /* prefill CTA work items, or decode split units x Hkv */
+  int32_t num_tile_pairs;     /* prefill: non-skipped (query tile, KV tile) pairs x heads/2 */
+  int32_t num_partial_pairs;
+  int32_t num_splits;         /* decode split units (before x Hkv) */
+} msa_plan_stats_t;
+
+/* Build a plan on the host (no CUDA call).  Inputs are host arrays, copied.
+ *   segs[num_segs]                      segment descriptors, any order
+ *   block_table[num_seqs * max_blocks_per_seq]  physical block of each logical block
+ *   block_pos[num_pool_blocks]          original position of token 0 of each block
+ *   block_fill[num_pool_blocks]         valid tokens of each block (1..16 when referenced)
+ *   cu_q[num_seqs+1], q_pos[cu_q[num_seqs]]  prefill: query rows of each sequence and
+ *                                       their original positions, strictly ascending per
+ *                                       sequence; decode: cu_q must be 0..num_seqs (one
+ *                                       query per sequence), q_pos may be NULL.
+ * Errors: INVALID_ARG, UNSUPPORTED, POS_OVERLAP (pool and chunk positions of one
+ * sequence repeat), BLOCK_OOB.  On error *out is NULL. */
+msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t mode, int32_t num_seqs,
+                             const msa_segment_t* segs, int32_t num_segs,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* block_pos, const int32_t* block_fill,
+                             int32_t num_pool_blocks,
+                             const int32_t* cu_q, const int32_t* q_pos,
+                             msa_plan_t** out);
+void msa_plan_destroy(msa_plan_t* plan);
+
+/* Bytes of the plan's device image; the caller allocates a device buffer of at least
+ * this size (16-byte aligned) and fills it with msa_plan_upload (async copy on
+ * `stream`; the plan must outlive the copy). */
+size_t msa_plan_device_bytes(const msa_plan_t* plan);
+msa_status_t msa_plan_upload(const msa_plan_t* plan, void* plan_dev, size_t bytes, cudaStream_t stream);
+
+/* Workspace: status word, scheduling counters and (decode) split partials.  The caller
+ * allocates msa_workspace_bytes (256-byte aligned) and calls msa_workspace_init once
+ * before first use (it zeroes the buffer on `stream`); the kernels leave it re-usable.
+ * A workspace must not be shared by launches that may overlap. */
+size_t msa_workspace_bytes(const msa_plan_t* plan);
+msa_status_t msa_workspace_init(void* workspace, size_t bytes, cudaStream_t stream);
+
+/* Canonical plan as int32 (the bit-exact indexing contract):
+ *   header  [mode, num_seqs, n_tok, n_kt, n_qt, n_cls]
+ *   n_tok x (src, id, offset, pos)     canonical KV order, each sequence in turn;
+ *                                      src 0 = pool (id = physical block, offset = slot),
+ *                                      src 1 = chunk (id = global query row, offset 0)
+ *   n_kt  x (seq, src, tok_begin, n_tok, minpos, maxpos)   prefill KV tiles: units of one
+ *                                      source in position order, <= 8 pool blocks or
+ *                                      <= 128 chunk tokens; new tile on source change
+ *   n_qt  x (seq, row0, nrows, minpos, maxpos)             query tiles of 128 rows
+ *   n_cls x class (0 SKIP, 1 FULL, 2 PARTIAL), per query tile, per KV tile of its sequence
+ * Decode plans export the tokens only (n_kt = n_qt = n_cls = 0).
+ * With out == NULL only *n (int32 count) is written.  WORKSPACE if capacity < *n. */
+msa_status_t msa_plan_export(const msa_plan_t* plan, int32_t* out, size_t capacity, size_t* n);
+
+/* Decode split units as int32 triples (seq, first canonical block, number of blocks). */
+msa_status_t msa_plan_export_splits(const msa_plan_t* plan, int32_t* out, size_t capacity, size_t* n);
+
+msa_status_t msa_plan_get_stats(const msa_plan_t* plan, msa_plan_stats_t* stats);
+
+/* Adaptive chunk tiler (abstract: an adaptive chunking scheduler keeps the hardware
+ * busy; the pages give no rule, this is the library's rule): for R recompute tokens
+ * take n = ceil(R/max_chunk) chunks of near-equal size rounded up to the 128-token
+ * tile, c = min(R, roundup(ceil(R/n),128)); cut front to back into ceil(R/c) chunks,
+ * the last taking the remainder; R < min_chunk gives one chunk.  max_chunk must be a
+ * positive multiple of 128.  Writes *n sizes (capacity permitting). */
+msa_status_t msa_chunk_sizes(int32_t R, int32_t min_chunk, int32_t max_chunk,
+                             int32_t* sizes, int32_t capacity, int32_t* n);
+
+/* MSA prefill (TTFT path), one launch for all sequences of the plan.
+ *   q        device bf16 [total_q][Hq][d]
+ *   k_chunk  device bf16 [total_q][Hkv][d], v_chunk likewise (the chunk's fresh K/V)
+ *   k_pool   device bf16 [num_pool_blocks][Hkv][16][d], v_pool likewise
+ *   out      device bf16 [total_q][Hq][d]; lse device fp32 [total_q][Hq]
+ *   scale    softmax scale (1/sqrt(d) for Eq. 1)
+ * All device pointers 16-byte aligned.  Errors: INVALID_ARG, MODE, WORKSPACE, CUDA. */
+msa_status_t msa_prefill(const msa_plan_t* plan, const void* plan_dev,
+                         const void* q, const void* k_chunk, const void* v_chunk,
+                         const void* k_pool, const void* v_pool,
+                         void* out, float* lse, float scale,
+                         void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* MSA decode (TPOT path): split-KV over the segments with the LSE merge fused in.
+ *   q   device bf16 [num_seqs][Hq][d]; out bf16 [num_seqs][Hq][d]; lse fp32 [num_seqs][Hq]
+ * Errors: INVALID_ARG, MODE, WORKSPACE, CUDA. */
+msa_status_t msa_decode(const msa_plan_t* plan, const void* plan_dev, const void* q,
+                        const void* k_pool, const void* v_pool,
+                        void* out, float* lse, float scale,
+                        void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Merge two partial attention results over disjoint key sets (elementwise over
+ * rows x heads): m = max(lse_a, lse_b), w = exp(lse - m), O = (w_a O_a + w_b O_b)/(w_a + w_b),
+ * LSE = m + ln(w_a + w_b); a part with lse = -inf weighs 0; both -inf give O = 0, LSE = -inf.
+ *   o_a, o_b  device fp32 [rows][heads][head_dim]; lse_a, lse_b fp32 [rows][heads]
+ *   o         device bf16 [rows][heads][head_dim]; lse fp32 [rows][heads]
+ * head_dim % 4 == 0.  Errors: INVALID_ARG, CUDA. */
+msa_status_t msa_merge_lse(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
+                           void* o, float* lse, int32_t rows, int32_t heads, int32_t head_dim,
+                           cudaStream_t stream);
+
+/* Gather the KV context of every sequence in canonical (position) order, bit-exact:
+ *   k_out, v_out device bf16 [n_tok][Hkv][d] in export order; pos_out int32 [n_tok] (nullable).
+ * k_chunk / v_chunk may be NULL for decode plans.  Errors: INVALID_ARG, WORKSPACE, CUDA. */
+msa_status_t msa_gather(const msa_plan_t* plan, const void* plan_dev,
+                        const void* k_chunk, const void* v_chunk,
+                        const void* k_pool, const void* v_pool,
+                        void* k_out, void* v_out, int32_t* pos_out, size_t out_tokens,
+                        cudaStream_t stream);
+
+/* Synchronise `stream`, read and clear the workspace status word.  Returns MSA_OK or
+ * the device-side error (e.g. MSA_ERR_TIMEOUT). */
+msa_status_t msa_get_status(void* workspace, cudaStream_t stream);
+
+/* Device-wait bound (spin iterations of each mbarrier wait before giving up with
+ * MSA_ERR_TIMEOUT); 0 restores the default.  Applies to later launches. */
+void msa_set_wait_limit(int64_t spins);
+
+const char* msa_status_string(msa_status_t status);
+int32_t msa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MSA_H_ */
