@@ -1,0 +1,290 @@
+"""Multi-Segment Attention (MSA) on one B300 -- thin Python binding of libmsa.so.
+
+The library (C ABI declared in include/msa.h) does all the work: the host planner and
+the sm_103a kernels.  This module only marshals arguments: numpy arrays for the layout,
+torch CUDA tensors for device memory and the current torch stream for ordering.  There
+is no fallback: if libmsa.so cannot be loaded every call raises.
+
+Paper: "Multi-Segment Attention: Enabling Efficient KV-Cache Management for Faster Large
+Language Model Serving" (Eq. 1; section 4.1; abstract).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmsa.so")
+
+MSA_PREFILL, MSA_DECODE = 0, 1
+STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "position overlap",
+          -4: "block out of range", -5: "workspace", -6: "cuda", -7: "timeout", -8: "mode"}
+
+
+class MSAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+class _Opts(ctypes.Structure):
+    _fields_ = [("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("decode_split_blocks", ctypes.c_int32), ("decode_min_ctas", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 4)]
+
+
+class _Stats(ctypes.Structure):
+    _fields_ = [("useful_flops", ctypes.c_int64), ("kv_tokens", ctypes.c_int64),
+                ("algorithmic_bytes", ctypes.c_int64), ("num_kv_tiles", ctypes.c_int32),
+                ("num_q_tiles", ctypes.c_int32), ("num_work_items", ctypes.c_int32),
+                ("num_tile_pairs", ctypes.c_int32), ("num_partial_pairs", ctypes.c_int32),
+                ("num_splits", ctypes.c_int32)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_SZ = ctypes.c_size_t
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+EXPORTS = {
+    # name: (restype, argtypes)
+    "msa_plan_create": (_I32, [ctypes.POINTER(_Opts), _I32, _I32, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P,
+                               ctypes.POINTER(_P)]),
+    "msa_plan_destroy": (None, [_P]),
+    "msa_plan_device_bytes": (_SZ, [_P]),
+    "msa_plan_upload": (_I32, [_P, _P, _SZ, _P]),
+    "msa_workspace_bytes": (_SZ, [_P]),
+    "msa_workspace_init": (_I32, [_P, _SZ, _P]),
+    "msa_plan_export": (_I32, [_P, _P, _SZ, ctypes.POINTER(_SZ)]),
+    "msa_plan_export_splits": (_I32, [_P, _P, _SZ, ctypes.POINTER(_SZ)]),
+    "msa_plan_get_stats": (_I32, [_P, ctypes.POINTER(_Stats)]),
+    "msa_chunk_sizes": (_I32, [_I32, _I32, _I32, _P, _I32, _I32P]),
+    "msa_prefill": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _SZ, _P]),
+    "msa_decode": (_I32, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _SZ, _P]),
+    "msa_merge_lse": (_I32, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P]),
+    "msa_gather": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "msa_get_status": (_I32, [_P, _P]),
+    "msa_set_wait_limit": (None, [ctypes.c_int64]),
+    "msa_status_string": (ctypes.c_char_p, [_I32]),
+    "msa_version": (_I32, []),
+}
+
+
+def lib():
+    """Load libmsa.so (raises if it is missing: there is no fallback path)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmsa.so is not built ({LIB_PATH}); run "
+                               "`python -m segmented_kv_attention_msa_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in EXPORTS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise MSAError(int(code), what)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream(stream=None) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def chunk_sizes(R: int, min_chunk: int, max_chunk: int) -> list:
+    """Adaptive chunk tiler of the library (see msa_chunk_sizes in include/msa.h)."""
+    n = ctypes.c_int32(0)
+    _check(lib().msa_chunk_sizes(R, min_chunk, max_chunk, None, 0, ctypes.byref(n)), "msa_chunk_sizes")
+    out = np.zeros(max(1, n.value), np.int32)
+    _check(lib().msa_chunk_sizes(R, min_chunk, max_chunk, _ptr(out), len(out), ctypes.byref(n)),
+           "msa_chunk_sizes")
+    return [int(x) for x in out[:n.value]]
+
+
+class Plan:
+    """Host plan (validated layout, tiles, work list) plus its device image."""
+
+    def __init__(self, mode: str, num_heads_q: int, num_heads_kv: int, head_dim: int,
+                 segments, block_table, block_pos, block_fill, cu_q, q_pos=None,
+                 decode_split_blocks: int = 0, decode_min_ctas: int = 0):
+        self.mode = mode
+        m = MSA_PREFILL if mode == "prefill" else MSA_DECODE
+        opts = _Opts(num_heads_q, num_heads_kv, head_dim, 16, decode_split_blocks, decode_min_ctas)
+        self._keep = [np.ascontiguousarray(np.asarray(x, np.int32)) for x in
+                      (segments, block_table, block_pos, block_fill, cu_q,
+                       q_pos if q_pos is not None else np.zeros(0, np.int32))]
+        seg, bt, bp, bf, cq, qp = self._keep
+        num_seqs = len(cq) - 1
+        h = ctypes.c_void_p(0)
+        _check(lib().msa_plan_create(ctypes.byref(opts), m, num_seqs, _ptr(seg), len(seg.reshape(-1, 3)),
+                                     _ptr(bt), bt.shape[1] if bt.ndim == 2 else 0, _ptr(bp), _ptr(bf),
+                                     len(bp), _ptr(cq), _ptr(qp) if qp.size else None, ctypes.byref(h)),
+               "msa_plan_create")
+        self._h = h
+        self.num_heads_q, self.num_heads_kv, self.head_dim = num_heads_q, num_heads_kv, head_dim
+        self.num_seqs = num_seqs
+        self.total_q = int(cq[-1])
+        self.dev = None
+        self.ws = None
+
+    @classmethod
+    def from_layout(cls, layout, **kw) -> "Plan":
+        return cls(layout.mode, layout.num_heads_q, layout.num_heads_kv, layout.head_dim,
+                   layout.segments, layout.block_table, layout.block_pos, layout.block_fill,
+                   layout.cu_q, layout.q_pos if layout.mode == "prefill" else None, **kw)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.msa_plan_destroy(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def device_bytes(self) -> int:
+        return int(lib().msa_plan_device_bytes(self._h))
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(lib().msa_workspace_bytes(self._h))
+
+    def export(self) -> np.ndarray:
+        n = ctypes.c_size_t(0)
+        _check(lib().msa_plan_export(self._h, None, 0, ctypes.byref(n)), "msa_plan_export")
+        out = np.zeros(n.value, np.int32)
+        _check(lib().msa_plan_export(self._h, _ptr(out), n.value, ctypes.byref(n)), "msa_plan_export")
+        return out
+
+    def export_splits(self) -> np.ndarray:
+        n = ctypes.c_size_t(0)
+        _check(lib().msa_plan_export_splits(self._h, None, 0, ctypes.byref(n)), "msa_plan_export_splits")
+        out = np.zeros(max(1, n.value), np.int32)
+        _check(lib().msa_plan_export_splits(self._h, _ptr(out), n.value, ctypes.byref(n)),
+               "msa_plan_export_splits")
+        return out[:n.value].reshape(-1, 3)
+
+    def stats(self) -> dict:
+        s = _Stats()
+        _check(lib().msa_plan_get_stats(self._h, ctypes.byref(s)), "msa_plan_get_stats")
+        return {f: int(getattr(s, f)) for f, _ in _Stats._fields_}
+
+    def upload(self, device="cuda", stream=None):
+        """Allocate the device image and workspace (torch) and fill them (library calls)."""
+        import torch
+        nb = max(256, self.device_bytes)
+        self.dev = torch.empty(nb, dtype=torch.uint8, device=device)
+        _check(lib().msa_plan_upload(self._h, _dptr(self.dev), nb, _stream(stream)), "msa_plan_upload")
+        wb = max(256, self.workspace_bytes)
+        self.ws = torch.empty(wb, dtype=torch.uint8, device=device)
+        _check(lib().msa_workspace_init(_dptr(self.ws), wb, _stream(stream)), "msa_workspace_init")
+        return self
+
+
+def _bf16(t, name):
+    import torch
+    if t is None:
+        return None
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    return t
+
+
+def prefill(plan: Plan, q, k_chunk, v_chunk, k_pool, v_pool, out=None, lse=None,
+            scale: Optional[float] = None, stream=None):
+    """MSA prefill; returns (out bf16 [Tq, Hq, d], lse fp32 [Tq, Hq])."""
+    import torch
+    for t, n in ((q, "q"), (k_chunk, "k_chunk"), (v_chunk, "v_chunk"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _bf16(t, n)
+    if plan.dev is None:
+        plan.upload(q.device, stream)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    scale = 1.0 / math.sqrt(plan.head_dim) if scale is None else float(scale)
+    _check(lib().msa_prefill(plan.handle, _dptr(plan.dev), _dptr(q), _dptr(k_chunk), _dptr(v_chunk),
+                             _dptr(k_pool), _dptr(v_pool), _dptr(out), _dptr(lse), scale,
+                             _dptr(plan.ws), plan.ws.numel(), _stream(stream)), "msa_prefill")
+    return out, lse
+
+
+def decode(plan: Plan, q, k_pool, v_pool, out=None, lse=None, scale: Optional[float] = None, stream=None):
+    """MSA decode (split-KV + LSE merge); returns (out bf16 [B, Hq, d], lse fp32 [B, Hq])."""
+    import torch
+    for t, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _bf16(t, n)
+    if plan.dev is None:
+        plan.upload(q.device, stream)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    scale = 1.0 / math.sqrt(plan.head_dim) if scale is None else float(scale)
+    _check(lib().msa_decode(plan.handle, _dptr(plan.dev), _dptr(q), _dptr(k_pool), _dptr(v_pool),
+                            _dptr(out), _dptr(lse), scale, _dptr(plan.ws), plan.ws.numel(), _stream(stream)),
+           "msa_decode")
+    return out, lse
+
+
+def merge_lse(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
+    """Merge two partial results (fp32 O [rows, H, d], fp32 LSE [rows, H]) -> bf16 O, fp32 LSE."""
+    import torch
+    rows, heads, d = o_a.shape
+    for t in (o_a, lse_a, o_b, lse_b):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("merge_lse inputs must be contiguous fp32 CUDA tensors")
+    if out is None:
+        out = torch.empty(rows, heads, d, dtype=torch.bfloat16, device=o_a.device)
+    if lse is None:
+        lse = torch.empty(rows, heads, dtype=torch.float32, device=o_a.device)
+    _check(lib().msa_merge_lse(_dptr(o_a), _dptr(lse_a), _dptr(o_b), _dptr(lse_b), _dptr(out), _dptr(lse),
+                               rows, heads, d, _stream(stream)), "msa_merge_lse")
+    return out, lse
+
+
+def gather(plan: Plan, k_chunk, v_chunk, k_pool, v_pool, stream=None):
+    """KV context of every sequence in canonical (position) order: (K, V, pos)."""
+    import torch
+    n = plan.stats()["kv_tokens"]
+    dev = k_pool.device
+    if plan.dev is None:
+        plan.upload(dev, stream)
+    k = torch.empty(max(1, n), plan.num_heads_kv, plan.head_dim, dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    pos = torch.empty(max(1, n), dtype=torch.int32, device=dev)
+    _check(lib().msa_gather(plan.handle, _dptr(plan.dev), _dptr(k_chunk), _dptr(v_chunk), _dptr(k_pool),
+                            _dptr(v_pool), _dptr(k), _dptr(v), _dptr(pos), k.shape[0], _stream(stream)),
+           "msa_gather")
+    return k[:n], v[:n], pos[:n]
+
+
+def get_status(plan: Plan, stream=None) -> int:
+    """Synchronise, read and clear the device status word of the plan's workspace."""
+    return int(lib().msa_get_status(_dptr(plan.ws), _stream(stream)))
+
+
+def set_wait_limit(ns: int):
+    lib().msa_set_wait_limit(int(ns))

@@ -1,0 +1,80 @@
+// Internal layout of the MSA plan: host object and the int32 records of its device
+// image.  Shared by the host planner and the kernels.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include "msa.h"
+
+#ifdef __cplusplus
+#include <vector>
+#endif
+
+namespace msa {
+
+constexpr int kBlock = 16;          // tokens per pool block
+constexpr int kTileRows = 128;      // tokens per KV tile / rows per query tile
+constexpr int kTileBlocks = kTileRows / kBlock;
+constexpr int kStatusBytes = 256;   // workspace head: status word + scheduling counters
+
+enum { SRC_POOL = 0, SRC_CHUNK = 1 };
+enum { CLS_SKIP = 0, CLS_FULL = 1, CLS_PARTIAL = 2 };
+
+// Query tile: `nrows` consecutive chunk rows of one sequence starting at global row
+// `row0`; its non-skipped KV tiles are list[list_begin, list_begin + list_count).
+struct QTileRec {
+  int32_t seq, row0, nrows, minpos, maxpos, list_begin, list_count, pad;
+};
+
+// KV tile.  Chunk tile: chunk rows [row0, row0 + ntok).  Pool tile: nblk blocks
+// blk[i] whose tokens sit at positions bpos[i] + t, t < bfill[i]; tile row 16*i + t.
+struct KTileRec {
+  int32_t src, ntok, row0, nblk, minpos, maxpos, full, pad;
+  int32_t blk[kTileBlocks];
+  int32_t bpos[kTileBlocks];
+  int32_t bfill[kTileBlocks];
+};
+
+// One prefill CTA work item: query tile `qt`, KV head `g`, query heads h0 .. h0+hpc-1.
+struct WorkRec {
+  int32_t qt, g, h0, cost;
+};
+
+// One decode split-KV unit: canonical blocks [blk_begin, blk_begin + blk_count) of the
+// flat block list, part `split_idx` of `nsplit` of sequence `seq`, whose first unit
+// has global index `first_split`.
+struct SplitRec {
+  int32_t seq, blk_begin, blk_count, split_idx, nsplit, first_split, ntok, pad;
+};
+
+// Gather unit: `n` tokens copied to output rows [out_row, out_row + n); pool block
+// `id` (slots 0..n-1, positions pos0 + t) or chunk rows id .. id+n-1.
+struct GatherRec {
+  int32_t src, id, n, out_row, pos0, pad0, pad1, pad2;
+};
+
+// Byte offsets of each section within the device image.
+struct DevLayout {
+  size_t qpos, qtile, ktile, list, work, split, blist, bfill, gather, total;
+};
+
+// Byte offsets within the workspace.
+struct WsLayout {
+  size_t status, counters, part_o, part_lse, total;
+};
+
+}  // namespace msa
+
+#ifdef __cplusplus
+struct msa_plan {
+  msa_mode_t mode;
+  int32_t num_seqs, Hq, Hkv, d, G, hpc, num_pool_blocks;
+  int32_t total_q, n_tok, n_qt, n_kt, n_list, n_work, n_split, n_blist, n_gather;
+  std::vector<int32_t> canon;       // canonical export
+  std::vector<int32_t> split_export;
+  std::vector<int32_t> image;       // device image (int32 words)
+  msa::DevLayout dev;
+  msa::WsLayout ws;
+  msa_plan_stats_t stats;
+};
+#endif

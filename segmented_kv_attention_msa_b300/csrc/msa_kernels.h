@@ -1,0 +1,69 @@
+// Parameter blocks and launchers of the MSA kernels (internal to libmsa.so).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "msa_internal.h"
+
+namespace msa {
+
+struct PrefillParams {
+  const int32_t* qpos;
+  const QTileRec* qt;
+  const KTileRec* kt;
+  const int32_t* list;
+  const WorkRec* work;
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* status;
+  int32_t n_work, Hq, Hkv, hpc;
+  int32_t pool_rows;  // rows of the pool tensor maps; a box starting here reads zeros
+  float scale_log2;
+  uint64_t wait_ns;
+};
+
+struct PrefillTensors {
+  const void *q, *k_chunk, *v_chunk, *k_pool, *v_pool;
+  int64_t total_q, num_pool_blocks;
+  int d;
+};
+
+struct DecodeParams {
+  const SplitRec* split;
+  const int32_t* blist;
+  const int32_t* bfill;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_pool;
+  const __nv_bfloat16* v_pool;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  int32_t* counters;
+  int32_t* status;
+  int32_t Hq, Hkv, G;
+  float scale_log2;
+  uint64_t wait_ns;
+};
+
+struct GatherParams {
+  const GatherRec* units;
+  const int32_t* qpos;
+  const uint4* k_chunk;
+  const uint4* v_chunk;
+  const uint4* k_pool;
+  const uint4* v_pool;
+  uint4* k_out;
+  uint4* v_out;
+  int32_t* pos_out;
+  int32_t Hkv;
+  int32_t d;
+};
+
+cudaError_t launch_prefill(const PrefillParams& p, const PrefillTensors& T, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int d, int n_split, cudaStream_t stream);
+cudaError_t launch_merge_lse(const float* oa, const float* la, const float* ob, const float* lb, void* o,
+                             float* lse, int64_t n_rh, int d, cudaStream_t stream);
+cudaError_t launch_gather(const GatherParams& p, int n_units, cudaStream_t stream);
+
+}  // namespace msa

@@ -1,0 +1,93 @@
+// Stand-alone LSE merge of two partial attention results, and the bit-exact gather
+// of each sequence's KV context into original-position order.
+#include <cuda_runtime.h>
+
+#include "msa_device.cuh"
+#include "msa_kernels.h"
+
+namespace msa {
+
+// Two attention results over disjoint key sets combine exactly through their
+// log-sum-exp: with m = max(lse_a, lse_b) and w = exp(lse - m),
+// O = (w_a O_a + w_b O_b) / (w_a + w_b), LSE = m + ln(w_a + w_b).
+// One thread per (row, head, 4 elements of d).
+__global__ void msa_merge_lse_kernel(const float4* __restrict__ oa, const float* __restrict__ la,
+                                     const float4* __restrict__ ob, const float* __restrict__ lb,
+                                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                     int64_t n_rh, int d4) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_rh * d4) return;
+  const int64_t rh = idx / d4;
+  const int c = (int)(idx % d4);
+  const float a = la[rh], b = lb[rh];
+  const float m = fmaxf(a, b);
+  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = -INFINITY;
+  if (m != -INFINITY) {
+    const float wa = (a == -INFINITY) ? 0.f : expf(a - m);
+    const float wb = (b == -INFINITY) ? 0.f : expf(b - m);
+    const float inv = 1.f / (wa + wb);
+    const float4 va = oa[idx], vb = ob[idx];
+    r.x = (wa * va.x + wb * vb.x) * inv;
+    r.y = (wa * va.y + wb * vb.y) * inv;
+    r.z = (wa * va.z + wb * vb.z) * inv;
+    r.w = (wa * va.w + wb * vb.w) * inv;
+    l = m + logf(wa + wb);
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(r.x, r.y), hi = __floats2bfloat162_rn(r.z, r.w);
+  uint2 packed;
+  packed.x = *reinterpret_cast<uint32_t*>(&lo);
+  packed.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(o)[idx] = packed;
+  if (c == 0) lse[rh] = l;
+}
+
+cudaError_t launch_merge_lse(const float* oa, const float* la, const float* ob, const float* lb, void* o,
+                             float* lse, int64_t n_rh, int d, cudaStream_t stream) {
+  const int d4 = d / 4;
+  const int64_t n = n_rh * d4;
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (n + threads - 1) / threads;
+  msa_merge_lse_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+      reinterpret_cast<const float4*>(oa), la, reinterpret_cast<const float4*>(ob), lb,
+      reinterpret_cast<__nv_bfloat16*>(o), lse, n_rh, d4);
+  return cudaGetLastError();
+}
+
+// Gather: one CTA per gather unit (a pool block or a run of consecutive chunk rows);
+// copies its tokens' K and V rows for every KV head with 16-byte moves.
+
+__global__ void msa_gather_kernel(const GatherParams p) {
+  const GatherRec u = p.units[blockIdx.x];
+  const int row_vec = p.d / 8;  // uint4 per (token, head) row
+  const int per_tok = p.Hkv * row_vec;
+  const int total = u.n * per_tok;
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int t = i / per_tok;
+    const int rem = i % per_tok;
+    const int g = rem / row_vec, c = rem % row_vec;
+    const size_t dst = ((size_t)(u.out_row + t) * p.Hkv + g) * row_vec + c;
+    size_t src;
+    if (u.src == SRC_POOL) {
+      src = (((size_t)u.id * p.Hkv + g) * kBlock + t) * row_vec + c;
+      p.k_out[dst] = p.k_pool[src];
+      p.v_out[dst] = p.v_pool[src];
+    } else {
+      src = ((size_t)(u.id + t) * p.Hkv + g) * row_vec + c;
+      p.k_out[dst] = p.k_chunk[src];
+      p.v_out[dst] = p.v_chunk[src];
+    }
+  }
+  if (p.pos_out)
+    for (int t = threadIdx.x; t < u.n; t += blockDim.x)
+      p.pos_out[u.out_row + t] = (u.src == SRC_POOL) ? u.pos0 + t : p.qpos[u.id + t];
+}
+
+cudaError_t launch_gather(const GatherParams& p, int n_units, cudaStream_t stream) {
+  if (n_units == 0) return cudaSuccess;
+  msa_gather_kernel<<<n_units, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

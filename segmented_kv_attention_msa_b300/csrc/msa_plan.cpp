@@ -1,0 +1,495 @@
+// Host planner of Multi-Segment Attention (MSA): validates segment descriptors and
+// the paged block table, puts every sequence's KV context (pool segments plus the
+// chunk's own tokens) in original-position order, cuts it into KV tiles, cuts the
+// chunk into query tiles, classifies each (query tile, KV tile) pair by position
+// (skip / full / partial), orders the CTA work list longest first, and splits decode
+// contexts into split-KV units.  No CUDA call is made here.
+//
+// Paper: "Multi-Segment Attention: Enabling Efficient KV-Cache Management for Faster
+// Large Language Model Serving", section 4.1 (a KV context of disjoint regions) and the
+// abstract (evicted blocks recomputed at their original positions; adaptive chunking).
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <numeric>
+#include <vector>
+
+#include "msa_internal.h"
+
+using namespace msa;
+
+namespace {
+
+struct Unit {  // pool block or chunk token, ordered by first position
+  int32_t first_pos, src, id, n;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+msa_status_t build_units(const msa_plan_opts_t* /*opts*/, msa_mode_t mode, int32_t num_seqs,
+                         const msa_segment_t* segs, int32_t num_segs, const int32_t* block_table,
+                         int32_t max_blocks, const int32_t* block_pos, const int32_t* block_fill,
+                         int32_t num_pool_blocks, const int32_t* cu_q, const int32_t* q_pos,
+                         std::vector<std::vector<Unit>>& units) {
+  units.assign(num_seqs, {});
+  for (int32_t i = 0; i < num_segs; ++i) {
+    const msa_segment_t& s = segs[i];
+    if (s.seq < 0 || s.seq >= num_seqs || s.num_blocks <= 0 || s.first_logical_block < 0)
+      return MSA_ERR_INVALID_ARG;
+    if ((int64_t)s.first_logical_block + s.num_blocks > max_blocks) return MSA_ERR_BLOCK_OOB;
+    const int32_t* row = block_table + (size_t)s.seq * max_blocks;
+    for (int32_t k = 0; k < s.num_blocks; ++k) {
+      int32_t b = row[s.first_logical_block + k];
+      if (b < 0 || b >= num_pool_blocks) return MSA_ERR_BLOCK_OOB;
+      int32_t f = block_fill[b], p = block_pos[b];
+      if (f < 1 || f > kBlock || p < 0 || p % kBlock != 0) return MSA_ERR_INVALID_ARG;
+      if (k + 1 < s.num_blocks) {
+        int32_t bn = row[s.first_logical_block + k + 1];
+        if (bn < 0 || bn >= num_pool_blocks) return MSA_ERR_BLOCK_OOB;
+        if (f != kBlock || block_pos[bn] != p + kBlock) return MSA_ERR_INVALID_ARG;
+      }
+      units[s.seq].push_back({p, SRC_POOL, b, f});
+    }
+  }
+  if (cu_q[0] != 0) return MSA_ERR_INVALID_ARG;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    int32_t r0 = cu_q[s], r1 = cu_q[s + 1];
+    if (r1 < r0) return MSA_ERR_INVALID_ARG;
+    if (mode == MSA_DECODE) {
+      if (r1 - r0 != 1) return MSA_ERR_INVALID_ARG;
+      continue;
+    }
+    for (int32_t r = r0; r < r1; ++r) {
+      if (q_pos[r] < 0) return MSA_ERR_INVALID_ARG;
+      if (r > r0 && q_pos[r] <= q_pos[r - 1]) return MSA_ERR_INVALID_ARG;
+      units[s].push_back({q_pos[r], SRC_CHUNK, r, 1});
+    }
+  }
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    auto& us = units[s];
+    std::sort(us.begin(), us.end(), [](const Unit& a, const Unit& b) {
+      if (a.first_pos != b.first_pos) return a.first_pos < b.first_pos;
+      if (a.src != b.src) return a.src < b.src;
+      return a.id < b.id;
+    });
+    for (size_t i = 1; i < us.size(); ++i)
+      if (us[i].first_pos <= us[i - 1].first_pos + us[i - 1].n - 1) return MSA_ERR_POS_OVERLAP;
+    if (mode == MSA_DECODE && us.empty()) return MSA_ERR_INVALID_ARG;
+  }
+  return MSA_OK;
+}
+
+struct KTileHost {
+  int32_t seq, src, tok_begin, ntok, minpos, maxpos, nunits;
+  int32_t first_unit;
+};
+
+}  // namespace
+
+extern "C" msa_status_t msa_chunk_sizes(int32_t R, int32_t min_chunk, int32_t max_chunk,
+                                        int32_t* sizes, int32_t capacity, int32_t* n) {
+  if (!n || R < 0 || min_chunk < 0 || max_chunk <= 0 || max_chunk % kTileRows != 0)
+    return MSA_ERR_INVALID_ARG;
+  std::vector<int32_t> out;
+  if (R > 0) {
+    if (R < min_chunk) {
+      out.push_back(R);
+    } else {
+      int64_t k0 = ceil_div(R, max_chunk);
+      int64_t c = ceil_div(R, k0);
+      c = std::min<int64_t>(R, ceil_div(c, kTileRows) * kTileRows);
+      int64_t k = ceil_div(R, c);
+      for (int64_t i = 0; i + 1 < k; ++i) out.push_back((int32_t)c);
+      out.push_back((int32_t)(R - c * (k - 1)));
+    }
+  }
+  *n = (int32_t)out.size();
+  if (sizes) {
+    if (capacity < (int32_t)out.size()) return MSA_ERR_WORKSPACE;
+    std::copy(out.begin(), out.end(), sizes);
+  }
+  return MSA_OK;
+}
+
+extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t mode,
+                                        int32_t num_seqs, const msa_segment_t* segs,
+                                        int32_t num_segs, const int32_t* block_table,
+                                        int32_t max_blocks, const int32_t* block_pos,
+                                        const int32_t* block_fill, int32_t num_pool_blocks,
+                                        const int32_t* cu_q, const int32_t* q_pos,
+                                        msa_plan_t** out) {
+  if (!out) return MSA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!opts || num_seqs <= 0 || num_segs < 0 || max_blocks < 0 || num_pool_blocks < 0 || !cu_q)
+    return MSA_ERR_INVALID_ARG;
+  if (mode != MSA_PREFILL && mode != MSA_DECODE) return MSA_ERR_INVALID_ARG;
+  if (num_segs > 0 && (!segs || !block_table || !block_pos || !block_fill)) return MSA_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)
+    if (opts->reserved[i] != 0) return MSA_ERR_INVALID_ARG;
+  const int32_t Hq = opts->num_heads_q, Hkv = opts->num_heads_kv, d = opts->head_dim;
+  if (Hq <= 0 || Hkv <= 0) return MSA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || (d != 64 && d != 128) || opts->block_size != kBlock) return MSA_ERR_UNSUPPORTED;
+  if (opts->decode_split_blocks < 0 || opts->decode_min_ctas < 0) return MSA_ERR_INVALID_ARG;
+  if (mode == MSA_PREFILL && cu_q[num_seqs] > 0 && !q_pos) return MSA_ERR_INVALID_ARG;
+
+  std::vector<std::vector<Unit>> units;
+  msa_status_t st = build_units(opts, mode, num_seqs, segs, num_segs, block_table, max_blocks,
+                                block_pos, block_fill, num_pool_blocks, cu_q, q_pos, units);
+  if (st != MSA_OK) return st;
+
+  msa_plan_t* P = new (std::nothrow) msa_plan_t();
+  if (!P) return MSA_ERR_INVALID_ARG;
+  P->mode = mode;
+  P->num_seqs = num_seqs;
+  P->Hq = Hq;
+  P->Hkv = Hkv;
+  P->d = d;
+  P->G = Hq / Hkv;
+  P->hpc = (P->G % 2 == 0) ? 2 : 1;
+  P->total_q = cu_q[num_seqs];
+  P->num_pool_blocks = num_pool_blocks;
+  std::memset(&P->stats, 0, sizeof(P->stats));
+
+  // ---- canonical token list
+  std::vector<int32_t> toks;
+  std::vector<int32_t> seq_tok_begin(num_seqs + 1, 0);
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    seq_tok_begin[s] = (int32_t)(toks.size() / 4);
+    for (const Unit& u : units[s])
+      for (int32_t t = 0; t < u.n; ++t) {
+        toks.push_back(u.src);
+        toks.push_back(u.id);
+        toks.push_back(u.src == SRC_POOL ? t : 0);
+        toks.push_back(u.first_pos + t);
+      }
+  }
+  seq_tok_begin[num_seqs] = (int32_t)(toks.size() / 4);
+  P->n_tok = seq_tok_begin[num_seqs];
+
+  std::vector<KTileHost> kts;
+  std::vector<QTileRec> qts;
+  std::vector<int32_t> cls;
+  std::vector<int32_t> seq_kt_begin(num_seqs + 1, 0);
+  if (mode == MSA_PREFILL) {
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      seq_kt_begin[s] = (int32_t)kts.size();
+      int32_t t_index = seq_tok_begin[s];
+      KTileHost cur{};
+      bool open = false;
+      for (size_t ui = 0; ui < units[s].size(); ++ui) {
+        const Unit& u = units[s][ui];
+        int32_t limit = u.src == SRC_POOL ? kTileBlocks : kTileRows;
+        if (!open || cur.src != u.src || cur.nunits >= limit) {
+          if (open) kts.push_back(cur);
+          cur = KTileHost{s, u.src, t_index, 0, u.first_pos, u.first_pos, 0, (int32_t)ui};
+          open = true;
+        }
+        cur.ntok += u.n;
+        cur.maxpos = u.first_pos + u.n - 1;
+        cur.nunits += 1;
+        t_index += u.n;
+      }
+      if (open) kts.push_back(cur);
+    }
+    seq_kt_begin[num_seqs] = (int32_t)kts.size();
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      for (int32_t a = cu_q[s]; a < cu_q[s + 1]; a += kTileRows) {
+        int32_t b = std::min(cu_q[s + 1], a + kTileRows);
+        QTileRec q{s, a, b - a, q_pos[a], q_pos[b - 1], 0, 0, 0};
+        for (int32_t k = seq_kt_begin[s]; k < seq_kt_begin[s + 1]; ++k) {
+          const KTileHost& t = kts[k];
+          int32_t c;
+          if (q.maxpos < t.minpos) c = CLS_SKIP;
+          else if (q.minpos >= t.maxpos && t.ntok == kTileRows) c = CLS_FULL;
+          else c = CLS_PARTIAL;
+          cls.push_back(c);
+        }
+        qts.push_back(q);
+      }
+    }
+  }
+  P->n_kt = (int32_t)kts.size();
+  P->n_qt = (int32_t)qts.size();
+
+  // ---- canonical export
+  P->canon = {(int32_t)mode, num_seqs, P->n_tok, P->n_kt, P->n_qt, (int32_t)cls.size()};
+  P->canon.insert(P->canon.end(), toks.begin(), toks.end());
+  for (const KTileHost& t : kts) {
+    int32_t r[6] = {t.seq, t.src, t.tok_begin, t.ntok, t.minpos, t.maxpos};
+    P->canon.insert(P->canon.end(), r, r + 6);
+  }
+  for (const QTileRec& q : qts) {
+    int32_t r[5] = {q.seq, q.row0, q.nrows, q.minpos, q.maxpos};
+    P->canon.insert(P->canon.end(), r, r + 5);
+  }
+  P->canon.insert(P->canon.end(), cls.begin(), cls.end());
+
+  // ---- statistics shared by both modes
+  int64_t pairs = 0;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    int32_t nt = seq_tok_begin[s + 1] - seq_tok_begin[s];
+    if (mode == MSA_DECODE) {
+      pairs += nt;
+      continue;
+    }
+    // visible keys of each query = keys with pos <= q_pos (tokens are sorted by pos)
+    const int32_t* tp = toks.data() + (size_t)seq_tok_begin[s] * 4;
+    int32_t j = 0;
+    for (int32_t r = cu_q[s]; r < cu_q[s + 1]; ++r) {
+      while (j < nt && tp[(size_t)j * 4 + 3] <= q_pos[r]) ++j;
+      pairs += j;
+    }
+  }
+  P->stats.useful_flops = pairs * (int64_t)Hq * 4 * d;
+  P->stats.kv_tokens = P->n_tok;
+  P->stats.num_kv_tiles = P->n_kt;
+  P->stats.num_q_tiles = P->n_qt;
+
+  // ---- device image
+  std::vector<int32_t> list;
+  std::vector<WorkRec> work;
+  std::vector<KTileRec> ktr(kts.size());
+  std::vector<SplitRec> splits;
+  std::vector<int32_t> blist, bfill;
+  std::vector<GatherRec> gather;
+
+  if (mode == MSA_PREFILL) {
+    for (size_t k = 0; k < kts.size(); ++k) {
+      const KTileHost& t = kts[k];
+      KTileRec& r = ktr[k];
+      std::memset(&r, 0, sizeof(r));
+      r.src = t.src;
+      r.ntok = t.ntok;
+      r.minpos = t.minpos;
+      r.maxpos = t.maxpos;
+      r.full = t.ntok == kTileRows;
+      if (t.src == SRC_CHUNK) {
+        r.row0 = units[t.seq][t.first_unit].id;
+        r.nblk = 0;
+      } else {
+        r.nblk = t.nunits;
+        for (int32_t i = 0; i < t.nunits; ++i) {
+          const Unit& u = units[t.seq][t.first_unit + i];
+          r.blk[i] = u.id;
+          r.bpos[i] = u.first_pos;
+          r.bfill[i] = u.n;
+        }
+      }
+    }
+    size_t ci = 0;
+    int64_t tile_pairs = 0, partial_pairs = 0;
+    for (size_t qi = 0; qi < qts.size(); ++qi) {
+      QTileRec& q = qts[qi];
+      q.list_begin = (int32_t)list.size();
+      int32_t s = q.seq;
+      int32_t cost = 0;
+      // full tiles first, then partial ones, each group in position order
+      for (int pass = 0; pass < 2; ++pass) {
+        for (int32_t k = seq_kt_begin[s]; k < seq_kt_begin[s + 1]; ++k) {
+          int32_t c = cls[ci + (k - seq_kt_begin[s])];
+          if (pass == 0 && c == CLS_FULL) list.push_back(k);
+          if (pass == 1 && c == CLS_PARTIAL) list.push_back(k | (int32_t)0x80000000u);
+        }
+      }
+      for (int32_t k = seq_kt_begin[s]; k < seq_kt_begin[s + 1]; ++k) {
+        int32_t c = cls[ci + (k - seq_kt_begin[s])];
+        if (c != CLS_SKIP) ++cost;
+        if (c == CLS_PARTIAL) ++partial_pairs;
+      }
+      ci += seq_kt_begin[s + 1] - seq_kt_begin[s];
+      q.list_count = (int32_t)list.size() - q.list_begin;
+      tile_pairs += q.list_count;
+      for (int32_t g = 0; g < Hkv; ++g)
+        for (int32_t h = 0; h < P->G; h += P->hpc)
+          work.push_back({(int32_t)qi, g, g * P->G + h, cost});
+    }
+    // longest first; ties keep (qt, g, h0) order
+    std::stable_sort(work.begin(), work.end(),
+                     [](const WorkRec& a, const WorkRec& b) { return a.cost > b.cost; });
+    P->stats.num_work_items = (int32_t)work.size();
+    P->stats.num_tile_pairs = (int32_t)(tile_pairs * (Hq / P->hpc));
+    P->stats.num_partial_pairs = (int32_t)(partial_pairs * (Hq / P->hpc));
+    int64_t bytes = 0;
+    bytes += (int64_t)P->total_q * Hq * d * 2 * 2;           // q read + out write
+    bytes += (int64_t)P->total_q * Hq * 4;                   // lse
+    bytes += (int64_t)P->n_tok * Hkv * d * 2 * 2;            // every KV token once, K and V
+    P->stats.algorithmic_bytes = bytes;
+  } else {
+    // decode: canonical block list and split-KV units
+    std::vector<int32_t> seq_blk_begin(num_seqs + 1, 0);
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      seq_blk_begin[s] = (int32_t)blist.size();
+      for (const Unit& u : units[s]) {
+        blist.push_back(u.id);
+        bfill.push_back(u.n);
+      }
+    }
+    seq_blk_begin[num_seqs] = (int32_t)blist.size();
+    int64_t total_blocks = (int64_t)blist.size();
+    int64_t S = opts->decode_split_blocks;
+    if (S == 0) {
+      int64_t target = opts->decode_min_ctas ? opts->decode_min_ctas : 16 * 148;
+      S = std::max<int64_t>(8, ceil_div(total_blocks * Hkv, target));
+    }
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      int32_t nb = seq_blk_begin[s + 1] - seq_blk_begin[s];
+      int32_t ns = (int32_t)ceil_div(nb, S);
+      int32_t per = (int32_t)ceil_div(nb, ns);
+      int32_t first = (int32_t)splits.size();
+      for (int32_t i = 0; i < ns; ++i) {
+        int32_t b0 = i * per, b1 = std::min(nb, b0 + per);
+        if (b1 <= b0) {
+          ns = i;
+          break;
+        }
+        int32_t ntok = 0;
+        for (int32_t b = b0; b < b1; ++b) ntok += bfill[seq_blk_begin[s] + b];
+        splits.push_back({s, seq_blk_begin[s] + b0, b1 - b0, i, 0, first, ntok, 0});
+      }
+      for (size_t i = first; i < splits.size(); ++i) splits[i].nsplit = (int32_t)(splits.size() - first);
+      for (size_t i = first; i < splits.size(); ++i) {
+        P->split_export.push_back(s);
+        P->split_export.push_back(splits[i].blk_begin - seq_blk_begin[s]);
+        P->split_export.push_back(splits[i].blk_count);
+      }
+    }
+    P->stats.num_splits = (int32_t)splits.size();
+    P->stats.num_work_items = (int32_t)splits.size() * Hkv;
+    int64_t bytes = 0;
+    bytes += (int64_t)P->n_tok * Hkv * d * 2 * 2;                 // K and V once
+    bytes += (int64_t)num_seqs * Hq * d * 2 * 2;                  // q read + out write
+    bytes += (int64_t)num_seqs * Hq * 4;                          // lse
+    bytes += total_blocks * 8;                                    // block id + fill
+    P->stats.algorithmic_bytes = bytes;
+  }
+  // gather units (both modes): one per pool block, one per run of chunk rows
+  {
+    int32_t out_row = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      const auto& us = units[s];
+      for (size_t i = 0; i < us.size(); ++i) {
+        const Unit& u = us[i];
+        if (u.src == SRC_POOL) {
+          gather.push_back({SRC_POOL, u.id, u.n, out_row, u.first_pos, 0, 0, 0});
+          out_row += u.n;
+        } else {
+          size_t j = i;
+          while (j + 1 < us.size() && us[j + 1].src == SRC_CHUNK && us[j + 1].id == us[j].id + 1 &&
+                 (j + 1 - i) < (size_t)kTileRows)
+            ++j;
+          int32_t n = (int32_t)(j - i + 1);
+          gather.push_back({SRC_CHUNK, u.id, n, out_row, u.first_pos, 0, 0, 0});
+          out_row += n;
+          i = j;
+        }
+      }
+    }
+  }
+
+  P->n_list = (int32_t)list.size();
+  P->n_work = (int32_t)work.size();
+  P->n_split = (int32_t)splits.size();
+  P->n_blist = (int32_t)blist.size();
+  P->n_gather = (int32_t)gather.size();
+
+  // ---- lay out the image (every section 256-byte aligned)
+  DevLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.qpos = take((size_t)P->total_q * 4);
+  L.qtile = take(qts.size() * sizeof(QTileRec));
+  L.ktile = take(ktr.size() * sizeof(KTileRec));
+  L.list = take(list.size() * 4);
+  L.work = take(work.size() * sizeof(WorkRec));
+  L.split = take(splits.size() * sizeof(SplitRec));
+  L.blist = take(blist.size() * 4);
+  L.bfill = take(bfill.size() * 4);
+  L.gather = take(gather.size() * sizeof(GatherRec));
+  L.total = std::max<size_t>(off, 256);
+  P->dev = L;
+  P->image.assign(L.total / 4, 0);
+  auto put = [&](size_t o, const void* src, size_t bytes) {
+    if (bytes) std::memcpy(reinterpret_cast<char*>(P->image.data()) + o, src, bytes);
+  };
+  if (mode == MSA_PREFILL && P->total_q) put(L.qpos, q_pos, (size_t)P->total_q * 4);
+  put(L.qtile, qts.data(), qts.size() * sizeof(QTileRec));
+  put(L.ktile, ktr.data(), ktr.size() * sizeof(KTileRec));
+  put(L.list, list.data(), list.size() * 4);
+  put(L.work, work.data(), work.size() * sizeof(WorkRec));
+  put(L.split, splits.data(), splits.size() * sizeof(SplitRec));
+  put(L.blist, blist.data(), blist.size() * 4);
+  put(L.bfill, bfill.data(), bfill.size() * 4);
+  put(L.gather, gather.data(), gather.size() * sizeof(GatherRec));
+
+  // ---- workspace layout
+  WsLayout W{};
+  size_t wo = 0;
+  W.status = 0;
+  wo = kStatusBytes;
+  W.counters = wo;
+  wo = align_up(wo + (size_t)num_seqs * Hq * 4, 256);
+  W.part_o = wo;
+  wo = align_up(wo + (size_t)P->n_split * Hq * d * 4, 256);
+  W.part_lse = wo;
+  wo = align_up(wo + (size_t)P->n_split * Hq * 4, 256);
+  W.total = wo;
+  P->ws = W;
+
+  *out = P;
+  return MSA_OK;
+}
+
+extern "C" void msa_plan_destroy(msa_plan_t* plan) { delete plan; }
+
+extern "C" size_t msa_plan_device_bytes(const msa_plan_t* plan) { return plan ? plan->dev.total : 0; }
+
+extern "C" size_t msa_workspace_bytes(const msa_plan_t* plan) { return plan ? plan->ws.total : 0; }
+
+extern "C" msa_status_t msa_plan_export(const msa_plan_t* plan, int32_t* out, size_t capacity,
+                                        size_t* n) {
+  if (!plan || !n) return MSA_ERR_INVALID_ARG;
+  *n = plan->canon.size();
+  if (!out) return MSA_OK;
+  if (capacity < plan->canon.size()) return MSA_ERR_WORKSPACE;
+  std::copy(plan->canon.begin(), plan->canon.end(), out);
+  return MSA_OK;
+}
+
+extern "C" msa_status_t msa_plan_export_splits(const msa_plan_t* plan, int32_t* out,
+                                               size_t capacity, size_t* n) {
+  if (!plan || !n) return MSA_ERR_INVALID_ARG;
+  *n = plan->split_export.size();
+  if (!out) return MSA_OK;
+  if (capacity < plan->split_export.size()) return MSA_ERR_WORKSPACE;
+  std::copy(plan->split_export.begin(), plan->split_export.end(), out);
+  return MSA_OK;
+}
+
+extern "C" msa_status_t msa_plan_get_stats(const msa_plan_t* plan, msa_plan_stats_t* stats) {
+  if (!plan || !stats) return MSA_ERR_INVALID_ARG;
+  *stats = plan->stats;
+  return MSA_OK;
+}
+
+extern "C" const char* msa_status_string(msa_status_t s) {
+  switch (s) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARG: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MSA_ERR_POS_OVERLAP: return "two KV tokens of one sequence share a position";
+    case MSA_ERR_BLOCK_OOB: return "block index out of range";
+    case MSA_ERR_WORKSPACE: return "buffer too small or misaligned";
+    case MSA_ERR_CUDA: return "CUDA error";
+    case MSA_ERR_TIMEOUT: return "device wait timed out";
+    case MSA_ERR_MODE: return "plan built for the other mode";
+  }
+  return "unknown status";
+}
+
+extern "C" int32_t msa_version(void) { return 1; }

@@ -1,0 +1,30 @@
+"""Shared helpers of the GPU parity tests."""
+import numpy as np
+
+ATOL, RTOL = 1e-2, 2e-2   # |gpu - ref| <= ATOL + RTOL * |ref| per element (out and lse)
+
+
+def np64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def assert_close(gpu, ref, what=""):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    both_inf = np.isneginf(gpu) & np.isneginf(ref)
+    g = np.where(both_inf, 0.0, gpu)
+    r = np.where(both_inf, 0.0, ref)
+    err = np.abs(g - r)
+    bad = ~(err <= ATOL + RTOL * np.abs(r))
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; first at "
+                             f"{tuple(i)}: gpu={gpu[tuple(i)]} ref={ref[tuple(i)]}; max abs err {err.max():.3e}")
+    return float(err.max()) if err.size else 0.0
+
+
+def workload_arrays(wl):
+    """Oracle inputs: the bf16 values of the workload as fp64 numpy arrays."""
+    return dict(q=np64(wl.q), k_chunk=np64(wl.k_chunk), v_chunk=np64(wl.v_chunk),
+                k_pool=np64(wl.k_pool), v_pool=np64(wl.v_pool))

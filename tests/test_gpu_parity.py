@@ -1,0 +1,318 @@
+"""GPU parity of the MSA kernels against the CPU oracle, called through the C ABI.
+
+Tolerance (bf16 inputs, fp32 accumulation): |gpu - oracle| <= 1e-2 + 2e-2 |oracle|
+per element on O and LSE.  Indexing (gather) is compared bit for bit, and so are two
+runs on the same data and two runs whose pool blocks sit at permuted physical ids.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import segmented_kv_attention_msa_b300 as msa
+from segmented_kv_attention_msa_b300 import build as B
+from segmented_kv_attention_msa_b300 import workload as W
+from oracle import msa_oracle as O
+from tests.helpers import assert_close, np64, workload_arrays
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    B.build()
+    msa.lib()
+
+
+def run_prefill(lay, wl=None, **kw):
+    wl = wl or W.make_values(lay, device="cuda")
+    plan = msa.Plan.from_layout(lay).upload("cuda")
+    out, lse = msa.prefill(plan, wl.q, wl.k_chunk, wl.v_chunk, wl.k_pool, wl.v_pool, **kw)
+    torch.cuda.synchronize()
+    assert msa.get_status(plan) == 0
+    return wl, out, lse
+
+
+def check_prefill(lay, rows=None, scale=None, wl=None):
+    wl, out, lse = run_prefill(lay, wl, scale=scale)
+    a = workload_arrays(wl)
+    sc = 1.0 / math.sqrt(lay.head_dim) if scale is None else scale
+    rows_, ref_o, ref_l = O.prefill(lay, a["q"], a["k_chunk"], a["v_chunk"], a["k_pool"], a["v_pool"], sc,
+                                    rows=rows)
+    assert_close(np64(out)[rows_], ref_o, "out")
+    assert_close(np64(lse)[rows_], ref_l, "lse")
+    return wl, out, lse
+
+
+# ----------------------------------------------------------------------------- merge / gather
+
+def test_merge_lse_kernel():
+    g = torch.Generator().manual_seed(3)
+    rows, H, d = 37, 5, 128
+    oa = torch.randn(rows, H, d, generator=g)
+    ob = torch.randn(rows, H, d, generator=g)
+    la = torch.randn(rows, H, generator=g) * 4
+    lb = torch.randn(rows, H, generator=g) * 4
+    la[0, 0] = -math.inf
+    lb[1, 1] = -math.inf
+    la[2, 2] = lb[2, 2] = -math.inf
+    o, l = msa.merge_lse(oa.cuda(), la.cuda(), ob.cuda(), lb.cuda())
+    ref_o, ref_l = O.merge_lse([oa.numpy(), ob.numpy()], [la.numpy(), lb.numpy()])
+    assert_close(np64(o), ref_o, "merged out")
+    assert_close(np64(l), ref_l, "merged lse")
+
+
+def test_decode_merge_invariant_gpu():
+    """Decode over segments A and over segments B, merged by msa_merge_lse, equals decode over A u B."""
+    specs = [W.SeqSpec([(0, 512), (512, 300), (1024, 77), (816, 208)], np.zeros(0)) for _ in range(3)]
+    lay = W.custom_decode(8, 2, 128, specs, seed=21, qk_std=0.6)
+    wl = W.make_values(lay, device="cuda")
+    plan = msa.Plan.from_layout(lay).upload("cuda")
+    whole_o, whole_l = msa.decode(plan, wl.q, wl.k_pool, wl.v_pool)
+    parts = []
+    for sel in (slice(0, None, 2), slice(1, None, 2)):
+        sub = W.Layout(**{**vars(lay), "segments": lay.segments[sel].copy()})
+        p = msa.Plan.from_layout(sub).upload("cuda")
+        o, l = msa.decode(p, wl.q, wl.k_pool, wl.v_pool)
+        parts.append((o.float().contiguous(), l))
+    mo, ml = msa.merge_lse(parts[0][0], parts[0][1], parts[1][0], parts[1][1])
+    torch.cuda.synchronize()
+    assert_close(np64(mo), np64(whole_o), "merged decode out")
+    assert_close(np64(ml), np64(whole_l), "merged decode lse")
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_gather_bit_exact(idx):
+    lay = W.make_layout(idx)
+    wl = W.make_values(lay, device="cuda")
+    plan = msa.Plan.from_layout(lay).upload("cuda")
+    k, v, pos = msa.gather(plan, wl.k_chunk, wl.v_chunk, wl.k_pool, wl.v_pool)
+    torch.cuda.synchronize()
+    a = workload_arrays(wl)
+    p_ref, k_ref, v_ref = O.gather_by_position(lay, 0, a["k_pool"], a["v_pool"], a["k_chunk"], a["v_chunk"])
+    np.testing.assert_array_equal(pos.cpu().numpy(), p_ref)
+    np.testing.assert_array_equal(np64(k), k_ref)
+    np.testing.assert_array_equal(np64(v), v_ref)
+
+
+def test_gather_decode_bit_exact():
+    lay = W.make_layout(4)
+    lay = W.Layout(**{**vars(lay)})
+    wl = W.make_values(lay, device="cuda")
+    plan = msa.Plan.from_layout(lay).upload("cuda")
+    k, v, pos = msa.gather(plan, None, None, wl.k_pool, wl.v_pool)
+    torch.cuda.synchronize()
+    a = workload_arrays(wl)
+    empty = np.zeros((0, lay.num_heads_kv, lay.head_dim))
+    off = 0
+    for s in range(lay.num_seqs):
+        p_ref, k_ref, v_ref = O.gather_by_position(lay, s, a["k_pool"], a["v_pool"], empty, empty)
+        n = len(p_ref)
+        if s in (0, 17, 63):
+            np.testing.assert_array_equal(pos[off:off + n].cpu().numpy(), p_ref)
+            np.testing.assert_array_equal(np64(k[off:off + n]), k_ref)
+            np.testing.assert_array_equal(np64(v[off:off + n]), v_ref)
+        off += n
+    assert off == k.shape[0]
+
+
+# ----------------------------------------------------------------------------- decode
+
+def check_decode(lay, seqs=None, **plan_kw):
+    wl = W.make_values(lay, device="cuda")
+    plan = msa.Plan.from_layout(lay, **plan_kw).upload("cuda")
+    out, lse = msa.decode(plan, wl.q, wl.k_pool, wl.v_pool)
+    torch.cuda.synchronize()
+    assert msa.get_status(plan) == 0
+    q = np64(wl.q)
+    kp, vp = np64(wl.k_pool), np64(wl.v_pool)
+    seqs_, ref_o, ref_l = O.decode(lay, q, kp, vp, 1.0 / math.sqrt(lay.head_dim), seqs=seqs)
+    assert_close(np64(out)[seqs_], ref_o, "decode out")
+    assert_close(np64(lse)[seqs_], ref_l, "decode lse")
+    return plan, out, lse
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 8, 128), (4, 2, 64), (16, 2, 128), (6, 3, 64)])
+@pytest.mark.parametrize("split", [0, 1, 3])
+def test_decode_small(Hq, Hkv, d, split):
+    rng = np.random.default_rng(Hq * 7 + d + split)
+    specs = []
+    for _ in range(5):
+        L = int(rng.integers(1, 900))
+        nb = -(-L // 16)
+        cuts = np.sort(rng.choice(np.arange(1, nb), size=min(nb - 1, int(rng.integers(0, 6))), replace=False)) \
+            if nb > 1 else np.array([], int)
+        edges = np.concatenate([[0], cuts, [nb]])
+        specs.append(W.SeqSpec([(int(a) * 16, min(int(b) * 16, L) - int(a) * 16)
+                                for a, b in zip(edges[:-1], edges[1:])], np.zeros(0)))
+    lay = W.custom_decode(Hq, Hkv, d, specs, seed=split, qk_std=1.0 / math.sqrt(d) * 4, shuffle_segments=True)
+    check_decode(lay, decode_split_blocks=split)
+
+
+def test_decode_sharp_logits():
+    specs = [W.SeqSpec([(0, 1000), (1008, 333)], np.zeros(0)) for _ in range(4)]
+    lay = W.custom_decode(32, 8, 128, specs, seed=5, qk_std=1.0)   # no 1/sqrt(d) pre-scaling
+    check_decode(lay, decode_split_blocks=8)
+
+
+def test_decode_workload4_sampled():
+    lay = W.make_layout(4)
+    Ls = [sum(lay.block_fill[lay.block_table[s, f + i]] for (q, f, nb) in lay.segments if q == s
+              for i in range(nb)) for s in range(lay.num_seqs)]
+    pick = sorted({int(np.argmax(Ls)), int(np.argmin(Ls)), 0, 7, 31, 63})
+    check_decode(lay, seqs=pick)
+
+
+def test_decode_deterministic_and_permutation_invariant():
+    specs = [W.SeqSpec([(0, 700), (704, 90)], np.zeros(0)) for _ in range(3)]
+    lay_a = W.custom_decode(8, 2, 128, specs, seed=1)
+    lay_b = W.custom_decode(8, 2, 128, specs, seed=2)     # other physical placement
+    wa = W.make_values(lay_a, device="cuda", seed=77)
+    # re-place the same logical values at lay_b's block ids
+    kb = torch.zeros(lay_b.num_pool_blocks, *wa.k_pool.shape[1:], dtype=wa.k_pool.dtype, device="cuda")
+    vb = torch.zeros_like(kb)
+    for (s, f, nb) in lay_a.segments:
+        for i in range(nb):
+            ba = int(lay_a.block_table[s, f + i])
+            pos = int(lay_a.block_pos[ba])
+            row_b = [x for x in lay_b.block_table[s] if x >= 0 and lay_b.block_pos[x] == pos and
+                     lay_b.block_fill[x] > 0]
+            kb[row_b[0]] = wa.k_pool[ba]
+            vb[row_b[0]] = wa.v_pool[ba]
+    pa = msa.Plan.from_layout(lay_a).upload("cuda")
+    pb = msa.Plan.from_layout(lay_b).upload("cuda")
+    o1, l1 = msa.decode(pa, wa.q, wa.k_pool, wa.v_pool)
+    o2, l2 = msa.decode(pa, wa.q, wa.k_pool, wa.v_pool)
+    o3, l3 = msa.decode(pb, wa.q, kb, vb)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+def test_decode_timeout_reports_status():
+    """A bounded wait that runs out returns MSA_ERR_TIMEOUT through the status word and
+    leaves the context usable (the copies in flight are drained before exit)."""
+    specs = [W.SeqSpec([(0, 4096)], np.zeros(0)) for _ in range(8)]
+    lay = W.custom_decode(8, 2, 128, specs, seed=3)
+    wl = W.make_values(lay, device="cuda")
+    plan = msa.Plan.from_layout(lay, decode_split_blocks=64).upload("cuda")
+    try:
+        msa.set_wait_limit(1)            # 1 ns: the first wait that is not already done gives up
+        msa.decode(plan, wl.q, wl.k_pool, wl.v_pool)
+        st = msa.get_status(plan)
+    finally:
+        msa.set_wait_limit(0)
+    assert st in (0, -7)
+    # re-arm the workspace (the aborted launch may leave merge counters set) and run again
+    plan.upload("cuda")
+    check = msa.decode(plan, wl.q, wl.k_pool, wl.v_pool)
+    torch.cuda.synchronize()
+    assert msa.get_status(plan) == 0
+    assert torch.isfinite(check[1]).all()
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def test_prefill_workload1_all_rows():
+    check_prefill(W.make_layout(1))
+
+
+def test_prefill_workload2_all_rows():
+    check_prefill(W.make_layout(2))
+
+
+def test_prefill_workload3_sampled():
+    lay = W.make_layout(3, tiler=msa.chunk_sizes)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(lay.total_q, 400, replace=False))
+    rows = np.unique(np.concatenate([rows, lay.cu_q[:-1], lay.cu_q[1:] - 1]))
+    check_prefill(lay, rows=rows)
+
+
+def test_prefill_workload5_sampled():
+    lay = W.make_layout(5)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([rng.choice(lay.total_q, 96, replace=False), [0, lay.total_q - 1]]))
+    check_prefill(lay, rows=rows)
+
+
+def _spec(pool_runs, chunk):
+    return W.SeqSpec(pool_runs, np.asarray(chunk))
+
+
+@pytest.mark.parametrize("case", ["no_cache", "prefix_only", "one_token", "single_segment",
+                                  "partial_blocks", "ragged_multi", "future_blocks", "tiny_tiles"])
+@pytest.mark.parametrize("heads", [(32, 8, 128), (4, 4, 64), (6, 2, 128), (3, 3, 64)])
+def test_prefill_edge_cases(case, heads):
+    Hq, Hkv, d = heads
+    rng = np.random.default_rng(hash(case) % 1000)
+    if case == "no_cache":
+        specs = [_spec([], np.arange(300))]
+    elif case == "prefix_only":
+        specs = [_spec([(0, 1024)], np.arange(1024, 1400))]
+    elif case == "one_token":
+        specs = [_spec([(0, 512), (528, 48)], [512]), _spec([(0, 16)], [16])]
+    elif case == "single_segment":
+        specs = [_spec([(256, 512)], np.concatenate([np.arange(0, 256), np.arange(768, 800)]))]
+    elif case == "partial_blocks":
+        specs = [_spec([(0, 37), (48, 100), (160, 9)], np.concatenate([np.arange(37, 48), np.arange(148, 160),
+                                                                       np.arange(169, 420)]))]
+    elif case == "ragged_multi":
+        specs = [W.random_prefill_spec(rng, int(rng.integers(2, 70)), 0.5, int(rng.integers(1, 200)),
+                                       int(rng.integers(1, 400))) for _ in range(5)]
+    elif case == "future_blocks":
+        specs = [_spec([(0, 128), (640, 512)], np.arange(128, 640))]
+    else:  # tiny_tiles: alternating single cached blocks and single chunk tokens
+        runs = [(32 * i, 16) for i in range(20)]
+        chunk = np.concatenate([np.arange(32 * i + 16, 32 * i + 17) for i in range(20)])
+        specs = [_spec(runs, chunk)]
+    lay = W.custom_prefill(Hq, Hkv, d, specs, seed=4, qk_std=1.0 / math.sqrt(d) * 3, shuffle_segments=True)
+    check_prefill(lay)
+
+
+def test_prefill_sharp_logits():
+    rng = np.random.default_rng(5)
+    spec = W.random_prefill_spec(rng, 64, 0.5, 200, 700)
+    lay = W.custom_prefill(16, 4, 128, [spec], seed=5, qk_std=1.0)
+    check_prefill(lay)
+
+
+def test_prefill_planted_maxima():
+    """Planted large logits at random keys force the running max to move across tiles."""
+    rng = np.random.default_rng(6)
+    spec = W.random_prefill_spec(rng, 80, 0.5, 300, 900)
+    lay = W.custom_prefill(8, 2, 128, [spec], seed=6, qk_std=0.2)
+    wl = W.make_values(lay, device="cuda")
+    nb = lay.num_pool_blocks
+    for _ in range(40):
+        b = int(rng.integers(0, nb))
+        t = int(rng.integers(0, 16))
+        wl.k_pool[b, :, t, :] = wl.q[int(rng.integers(0, lay.total_q)), :2, :].mean(0) * 6
+    for _ in range(10):
+        r = int(rng.integers(0, lay.total_q))
+        wl.k_chunk[r] = wl.q[r, ::4, :] * 6
+    check_prefill(lay, wl=wl)
+
+
+def test_prefill_deterministic_and_permutation_invariant():
+    rng = np.random.default_rng(8)
+    spec = W.random_prefill_spec(rng, 60, 0.6, 150, 600)
+    lay_a = W.custom_prefill(8, 2, 128, [spec], seed=11)
+    lay_b = W.custom_prefill(8, 2, 128, [spec], seed=12)
+    wa = W.make_values(lay_a, device="cuda", seed=5)
+    kb = torch.zeros(lay_b.num_pool_blocks, *wa.k_pool.shape[1:], dtype=torch.bfloat16, device="cuda")
+    vb = torch.zeros_like(kb)
+    pos_to_b = {int(lay_b.block_pos[x]): int(x) for x in lay_b.block_table[0] if x >= 0}
+    for x in lay_a.block_table[0]:
+        if x >= 0:
+            kb[pos_to_b[int(lay_a.block_pos[x])]] = wa.k_pool[x]
+            vb[pos_to_b[int(lay_a.block_pos[x])]] = wa.v_pool[x]
+    pa = msa.Plan.from_layout(lay_a).upload("cuda")
+    pb = msa.Plan.from_layout(lay_b).upload("cuda")
+    o1, l1 = msa.prefill(pa, wa.q, wa.k_chunk, wa.v_chunk, wa.k_pool, wa.v_pool)
+    o2, l2 = msa.prefill(pa, wa.q, wa.k_chunk, wa.v_chunk, wa.k_pool, wa.v_pool)
+    o3, l3 = msa.prefill(pb, wa.q, wa.k_chunk, wa.v_chunk, kb, vb)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)

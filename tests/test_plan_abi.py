@@ -1,0 +1,200 @@
+"""Host-side checks of libmsa.so (no GPU needed): every symbol declared in
+include/msa.h is exported, the planner's canonical plan equals the oracle's bit for
+bit, the chunk tiler equals the oracle's rule, decode splits partition the context,
+useful-FLOP counts agree, and malformed layouts return the documented error codes."""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import segmented_kv_attention_msa_b300 as msa
+from segmented_kv_attention_msa_b300 import build as B
+from segmented_kv_attention_msa_b300 import workload as W
+from oracle import msa_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    B.build()
+    return msa.lib()
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "msa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_symbols_exported():
+    syms = header_symbols()
+    assert len(syms) >= 18
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (msa_\w+)", out))
+    missing = [s for s in syms if s not in exported]
+    assert not missing, missing
+    # and the binding declares them all
+    assert set(syms) <= set(msa.EXPORTS)
+
+
+def test_version():
+    assert msa.lib().msa_version() == 1
+
+
+@pytest.mark.parametrize("idx", [1, 2, 5])
+def test_plan_export_bit_exact(idx):
+    lay = W.make_layout(idx)
+    plan = msa.Plan.from_layout(lay)
+    np.testing.assert_array_equal(plan.export(), O.canonical_plan(lay))
+
+
+def test_plan_export_multiturn():
+    lay = W.make_layout(3, tiler=O.chunk_sizes)
+    lay2 = W.make_layout(3, tiler=msa.chunk_sizes)
+    np.testing.assert_array_equal(lay.q_pos, lay2.q_pos)
+    np.testing.assert_array_equal(lay.block_table, lay2.block_table)
+    plan = msa.Plan.from_layout(lay)
+    np.testing.assert_array_equal(plan.export(), O.canonical_plan(lay))
+
+
+def test_plan_hand_example():
+    from tests.test_oracle_pins import hand_expected, hand_layout
+    plan = msa.Plan.from_layout(hand_layout())
+    np.testing.assert_array_equal(plan.export(), hand_expected())
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_plan_random_layouts(seed):
+    rng = np.random.default_rng(100 + seed)
+    specs = [W.random_prefill_spec(rng, int(rng.integers(1, 40)), float(rng.random()),
+                                   int(rng.integers(1, 300)), int(rng.integers(1, 700)))
+             for _ in range(int(rng.integers(1, 5)))]
+    lay = W.custom_prefill(8, 2, 64, specs, seed=seed, shuffle_segments=True)
+    plan = msa.Plan.from_layout(lay)
+    np.testing.assert_array_equal(plan.export(), O.canonical_plan(lay))
+    assert plan.stats()["useful_flops"] == O.useful_flops(lay)
+
+
+def test_decode_plan_tokens_and_splits():
+    lay = W.make_layout(4)
+    plan = msa.Plan.from_layout(lay)
+    np.testing.assert_array_equal(plan.export(), O.canonical_plan(lay))
+    sp = plan.export_splits()
+    # splits partition each sequence's canonical block list, in order, none empty
+    for s in range(lay.num_seqs):
+        mine = sp[sp[:, 0] == s]
+        nblk = sum(int(nb) for (q, f, nb) in lay.segments if q == s)
+        assert mine[0, 1] == 0 and np.all(mine[:, 2] > 0)
+        assert np.all(mine[1:, 1] == mine[:-1, 1] + mine[:-1, 2])
+        assert mine[-1, 1] + mine[-1, 2] == nblk
+    st = plan.stats()
+    assert st["useful_flops"] == O.useful_flops(lay)
+    assert st["num_work_items"] >= 2 * 148
+
+
+def test_chunk_tiler_matches_oracle():
+    rng = np.random.default_rng(1)
+    for _ in range(3000):
+        hi = 128 * int(rng.integers(1, 40))
+        lo = int(rng.integers(0, hi + 1))
+        R = int(rng.integers(0, 20 * hi))
+        assert msa.chunk_sizes(R, lo, hi) == O.chunk_sizes(R, lo, hi)
+
+
+def test_chunk_tiler_rejects_bad_max():
+    with pytest.raises(msa.MSAError):
+        msa.chunk_sizes(1000, 10, 100)
+
+
+# ----------------------------------------------------------------------------- validation
+
+def base_layout():
+    from tests.test_oracle_pins import hand_layout
+    return hand_layout()
+
+
+def make(lay, **kw):
+    args = dict(mode=lay.mode, num_heads_q=lay.num_heads_q, num_heads_kv=lay.num_heads_kv,
+                head_dim=lay.head_dim, segments=lay.segments, block_table=lay.block_table,
+                block_pos=lay.block_pos, block_fill=lay.block_fill, cu_q=lay.cu_q, q_pos=lay.q_pos)
+    args.update(kw)
+    return msa.Plan(**args)
+
+
+def expect(code, **kw):
+    with pytest.raises(msa.MSAError) as e:
+        make(base_layout(), **kw)
+    assert e.value.code == code
+
+
+def test_validation_ok():
+    make(base_layout())
+
+
+def test_unsupported_head_dim():
+    expect(-2, head_dim=96)
+
+
+def test_unsupported_gqa():
+    expect(-2, num_heads_q=3, num_heads_kv=2)
+
+
+def test_block_out_of_range():
+    lay = base_layout()
+    bt = lay.block_table.copy()
+    bt[0, 3] = 99
+    expect(-4, block_table=bt)
+
+
+def test_logical_block_out_of_row():
+    lay = base_layout()
+    seg = lay.segments.copy()
+    seg[0, 2] = 5
+    expect(-4, segments=seg)
+
+
+def test_position_overlap_pool_vs_chunk():
+    lay = base_layout()
+    qp = lay.q_pos.copy()
+    qp[0] = 150         # inside the cached block at 144..159
+    qp = np.sort(qp)
+    expect(-3, q_pos=qp)
+
+
+def test_position_overlap_two_blocks():
+    lay = base_layout()
+    bp = lay.block_pos.copy()
+    bp[0] = 176         # block 0 now starts where block 7 does
+    expect(-3, block_pos=bp)
+
+
+def test_unsorted_q_pos():
+    lay = base_layout()
+    qp = lay.q_pos.copy()
+    qp[[2, 3]] = qp[[3, 2]]
+    expect(-1, q_pos=qp)
+
+
+def test_inconsistent_run():
+    lay = base_layout()
+    bp = lay.block_pos.copy()
+    bp[10] = 320        # second block of the first segment no longer follows the first
+    expect(-1, block_pos=bp)
+
+
+def test_partial_block_inside_run():
+    lay = base_layout()
+    bf = lay.block_fill.copy()
+    bf[13] = 8          # first block of an 8-block run may not be partial
+    expect(-1, block_fill=bf)
+
+
+def test_decode_needs_one_query_per_sequence():
+    lay = W.custom_decode(4, 2, 64, [W.SeqSpec([(0, 40)], np.zeros(0))], seed=0)
+    with pytest.raises(msa.MSAError) as e:
+        msa.Plan("decode", 4, 2, 64, lay.segments, lay.block_table, lay.block_pos, lay.block_fill,
+                 np.array([0, 2], np.int32))
+    assert e.value.code == -1
