@@ -1,0 +1,435 @@
+"""Benchmark of the MSA hot path on B300.
+
+One step = one MSA prefill launch over the Llama-3-8B-shaped attention layer workload
+(32/8 heads, d = 128, 8192-token context in 16-token blocks, 60% cached in 3-10 runs,
+2048-token query chunk) followed by one MSA decode launch over the batch-64 decode
+workload (32/8 heads, contexts 4k-64k split into 2-32 scattered segments), both on
+inputs resident in HBM.  The plan (host planner) is built and uploaded before timing.
+
+value        = useful prefill TFLOP/s (4 d Hq per visible query/key pair) over the timed
+               prefill launches; the decode's algorithmic HBM GB/s is in "decode".
+roofline     = prefill kernel vs the measured dense bf16 peak; decode.roofline = decode
+               kernel vs the measured HBM copy bandwidth.
+e2e          = the same metrics with the step's inputs copied from pinned host memory and
+               its results read back inside the timed region (the KV pool and the plan
+               stay resident: they are the cache).
+cpu_baseline = the CPU oracle timed on this host on a bounded sample of the same workload.
+
+`--impl reference` times the CPU oracle as the reference arm (there is no other
+implementation of this method to run).
+Multi-GPU: replicas only -- each rank runs its own copy of the step with no collective
+on the data path; a barrier and a max-reduction of the timings bracket the run.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MSA prefill useful TFLOPS (% bf16 TC peak); decode HBM GB/s (% peak), 1 B300"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_traffic(name: str, src_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current source of the kernel (sha256 of its .cu file); otherwise None."""
+    summ = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
+    src = os.path.join(ROOT, "segmented_kv_attention_msa_b300", "csrc", src_file)
+    try:
+        kv = {}
+        for line in open(summ):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if kv.get("source_sha256") != sha:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("MSA_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def reduce_max(values, world, device=None):
+    """Element-wise max over ranks (used for the per-step timings)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(per_rank_units, max_seconds):
+    """Whole-job throughput: units processed by all ranks / slowest rank's time."""
+    return sum(per_rank_units) / max_seconds if max_seconds > 0 else 0.0
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import segmented_kv_attention_msa_b300 as msa
+    from segmented_kv_attention_msa_b300 import build as B
+    from segmented_kv_attention_msa_b300 import workload as W
+
+    if not os.path.exists(msa.LIB_PATH):
+        B.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_kind = load_peaks()
+
+    # ---- prefill workload (the metric's configuration) and decode workload
+    pl = W.make_layout(args.workload, tiler=msa.chunk_sizes)
+    pw = W.make_values(pl, device=dev)
+    pplan = msa.Plan.from_layout(pl).upload(dev)
+    pst = pplan.stats()
+    pout = torch.empty_like(pw.q)
+    plse = torch.empty(pw.q.shape[0], pw.q.shape[1], dtype=torch.float32, device=dev)
+
+    dl = W.make_layout(args.decode_workload)
+    dw = W.make_values(dl, device=dev)
+    dplan = msa.Plan.from_layout(dl).upload(dev)
+    dst = dplan.stats()
+    dout = torch.empty_like(dw.q)
+    dlse = torch.empty(dw.q.shape[0], dw.q.shape[1], dtype=torch.float32, device=dev)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MB > 126 MB L2
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        msa.prefill(pplan, pw.q, pw.k_chunk, pw.v_chunk, pw.k_pool, pw.v_pool, out=pout, lse=plse)
+        if ev is not None:
+            ev[1].record()
+        msa.decode(dplan, dw.q, dw.k_pool, dw.v_pool, out=dout, lse=dlse)
+        if ev is not None:
+            ev[2].record()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if msa.get_status(pplan) != 0 or msa.get_status(dplan) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        step(evs[k])
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    if msa.get_status(pplan) != 0 or msa.get_status(dplan) != 0:
+        raise RuntimeError("device error during the timed steps")
+    pf_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)]
+    dc_ms = [evs[k][1].elapsed_time(evs[k][2]) for k in range(args.steps)]
+    pf_mean, dc_mean = statistics.mean(pf_ms), statistics.mean(dc_ms)
+    pf_mean, dc_mean = reduce_max([pf_mean, dc_mean], world, dev)
+
+    flops = pst["useful_flops"]
+    dbytes = dst["algorithmic_bytes"]
+    value = aggregate([flops] * world, pf_mean * 1e-3) / 1e12
+    dec_gbs = aggregate([dbytes] * world, dc_mean * 1e-3) / 1e9
+    tc_peak = peaks["bf16_tflops"]
+    hbm_peak = peaks["hbm_gbs"]
+    pf_ach = flops / (pf_mean * 1e-3) / 1e12
+    dc_ach = dbytes / (dc_mean * 1e-3) / 1e9
+
+    # ---- end to end: inputs from pinned host memory, results read back, every step
+    hq = pw.q.cpu().pin_memory()
+    hkc = pw.k_chunk.cpu().pin_memory()
+    hvc = pw.v_chunk.cpu().pin_memory()
+    hout = torch.empty(pout.shape, dtype=pout.dtype).pin_memory()
+    hlse = torch.empty(plse.shape, dtype=plse.dtype).pin_memory()
+    hdq = dw.q.cpu().pin_memory()
+    hdout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    hdlse = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
+    dq_dev, kc_dev, vc_dev = torch.empty_like(pw.q), torch.empty_like(pw.k_chunk), torch.empty_like(pw.v_chunk)
+    ddq_dev = torch.empty_like(dw.q)
+    e2e_steps = max(1, min(args.steps, 10))
+    pe = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e2e_steps)]
+    torch.cuda.synchronize()
+    for k in range(e2e_steps):
+        flush.fill_(k & 0xFF)
+        pe[k][0].record()
+        dq_dev.copy_(hq, non_blocking=True)
+        kc_dev.copy_(hkc, non_blocking=True)
+        vc_dev.copy_(hvc, non_blocking=True)
+        msa.prefill(pplan, dq_dev, kc_dev, vc_dev, pw.k_pool, pw.v_pool, out=pout, lse=plse)
+        hout.copy_(pout, non_blocking=True)
+        hlse.copy_(plse, non_blocking=True)
+        pe[k][1].record()
+        ddq_dev.copy_(hdq, non_blocking=True)
+        msa.decode(dplan, ddq_dev, dw.k_pool, dw.v_pool, out=dout, lse=dlse)
+        hdout.copy_(dout, non_blocking=True)
+        hdlse.copy_(dlse, non_blocking=True)
+        pe[k][2].record()
+    torch.cuda.synchronize()
+    e2e_pf = statistics.mean(pe[k][0].elapsed_time(pe[k][1]) for k in range(e2e_steps))
+    e2e_dc = statistics.mean(pe[k][1].elapsed_time(pe[k][2]) for k in range(e2e_steps))
+    e2e_pf, e2e_dc = reduce_max([e2e_pf, e2e_dc], world, dev)
+    h2d_pf = sum(t.numel() * t.element_size() for t in (hq, hkc, hvc))
+    d2h_pf = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+    h2d_dc = hdq.numel() * hdq.element_size()
+    d2h_dc = hdout.numel() * hdout.element_size() + hdlse.numel() * hdlse.element_size()
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(pf_mean + dc_mean, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded generator; the paper's datasets are not available)",
+        "config": {
+            "workload": pl.name, "decode_workload": dl.name,
+            "prefill": {"num_heads_q": pl.num_heads_q, "num_heads_kv": pl.num_heads_kv, "head_dim": pl.head_dim,
+                        "query_tokens": pl.total_q, "kv_tokens": pst["kv_tokens"],
+                        "segments": int(len(pl.segments)), "useful_flops": flops,
+                        "kv_tiles": pst["num_kv_tiles"], "tile_pairs": pst["num_tile_pairs"],
+                        "partial_pairs": pst["num_partial_pairs"]},
+            "decode": {"batch": dl.num_seqs, "num_heads_q": dl.num_heads_q, "num_heads_kv": dl.num_heads_kv,
+                       "head_dim": dl.head_dim, "kv_tokens": dst["kv_tokens"], "segments": int(len(dl.segments)),
+                       "splits": dst["num_splits"], "algorithmic_bytes": dbytes},
+            "l2": "flushed between steps (256 MB write)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {"bound": "tensor", "achieved": round(pf_ach, 2), "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": round(pf_ach / tc_peak, 4), "traffic": kernel_traffic("prefill", "msa_prefill.cu"),
+                     "kernel": "msa_prefill_kernel<128>", "peak_source": f"{peak_kind} bf16_tflops (burst)"},
+        "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "ms": round(dc_mean, 4),
+                   "roofline": {"bound": "hbm", "achieved": round(dc_ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                                "frac": round(dc_ach / hbm_peak, 4),
+                                "traffic": kernel_traffic("decode", "msa_decode.cu"),
+                                "kernel": "msa_decode_kernel<128,4>", "peak_source": f"{peak_kind} hbm_gbs"},
+                   "e2e": {"value": round(dbytes / (e2e_dc * 1e-3) / 1e9, 1), "unit": "GB/s",
+                           "h2d_bytes_per_step": h2d_dc, "d2h_bytes_per_step": d2h_dc}},
+        "prefill_ms": round(pf_mean, 4),
+        "e2e": {"value": round(flops * world / (e2e_pf * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d_pf + h2d_dc, "d2h_bytes_per_step": d2h_pf + d2h_dc,
+                "prefill_ms": round(e2e_pf, 4), "decode_ms": round(e2e_dc, 4)},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+        "wall_s": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(pl, pw, args.cpu_rows)
+    return result
+
+
+# ----------------------------------------------------------------------------- the oracle as baseline
+
+def oracle_prefill_sample(pl, arrays, rows):
+    from oracle import msa_oracle as O
+    t0 = time.perf_counter()
+    O.prefill(pl, arrays["q"], arrays["k_chunk"], arrays["v_chunk"], arrays["k_pool"], arrays["v_pool"],
+              1.0 / math.sqrt(pl.head_dim), rows=rows)
+    return time.perf_counter() - t0
+
+
+def sample_flops(pl, rows):
+    """Useful FLOPs of the sampled query rows (visible pairs x 4 d Hq), counted directly."""
+    import numpy as np
+    total = 0
+    for s in range(pl.num_seqs):
+        pos = []
+        for (q, f, nb) in pl.segments:
+            if q != s:
+                continue
+            for i in range(nb):
+                b = pl.block_table[s, f + i]
+                pos.extend(range(int(pl.block_pos[b]), int(pl.block_pos[b]) + int(pl.block_fill[b])))
+        pos.extend(pl.q_pos[pl.cu_q[s]:pl.cu_q[s + 1]].tolist())
+        pos = np.sort(np.array(pos))
+        sel = [r for r in rows if pl.cu_q[s] <= r < pl.cu_q[s + 1]]
+        total += int(np.searchsorted(pos, pl.q_pos[sel], side="right").sum())
+    return total * pl.num_heads_q * 4 * pl.head_dim
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(pl, pw, n_rows):
+    import numpy as np
+    arrays = {k: getattr(pw, k).float().cpu().numpy().astype(np.float64)
+              for k in ("q", "k_chunk", "v_chunk", "k_pool", "v_pool")}
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(pl.total_q, min(n_rows, pl.total_q), replace=False))
+    secs = oracle_prefill_sample(pl, arrays, rows)
+    fl = sample_flops(pl, rows)
+    return {"value": round(fl / secs / 1e12, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{len(rows)} of {pl.total_q} query rows of {pl.name}, all {pl.num_heads_q} heads, "
+                      f"fp64 numpy ({secs:.2f} s)"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle, timed on this host, on a bounded sample per step."""
+    if rank != 0:
+        return None
+    import numpy as np
+    from segmented_kv_attention_msa_b300 import workload as W
+    pl = W.make_layout(args.workload, tiler=_oracle_tiler())
+    pw = W.make_values(pl, device="cpu")
+    arrays = {k: getattr(pw, k).float().numpy().astype(np.float64)
+              for k in ("q", "k_chunk", "v_chunk", "k_pool", "v_pool")}
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(pl.total_q, min(args.ref_rows, pl.total_q), replace=False))
+    for _ in range(args.warmup):
+        oracle_prefill_sample(pl, arrays, rows[:8])
+    t = [oracle_prefill_sample(pl, arrays, rows) for _ in range(args.steps)]
+    fl = sample_flops(pl, rows)
+    v = fl / statistics.mean(t) / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(t) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator)",
+        "config": {"workload": pl.name, "sample_rows": len(rows)},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{len(rows)} of {pl.total_q} query rows per step, all heads"},
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def _oracle_tiler():
+    from oracle import msa_oracle as O
+    return O.chunk_sizes
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=2, help="prefill workload (1, 2, 3 or 5)")
+    ap.add_argument("--decode-workload", type=int, default=4)
+    ap.add_argument("--cpu-rows", type=int, default=2048)
+    ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_ours(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
