@@ -169,6 +169,25 @@ msa_status_t msa_decode(const msa_plan_t* plan, const void* plan_dev, const void
                         void* out, float* lse, float scale,
                         void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* Decode without any device allocation.  The paper has no counterpart: this is a
+ * convenience of this library for callers that cannot allocate device memory -- e.g. a
+ * serving engine that reserves almost all of HBM for its KV-cache pool when it starts and
+ * hands out nothing afterwards, or a latency-critical loop that must not call cudaMalloc or
+ * cudaFree because they can synchronise the whole device.  Same inputs, outputs and result
+ * as msa_decode, but no workspace argument: the split-KV scratch lives in one fixed 8 MiB
+ * device array owned by the library (every GPU that loads libmsa.so holds it until the
+ * process exits).  Plans whose msa_workspace_bytes exceed 8 MiB are rejected with
+ * MSA_ERR_WORKSPACE.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture.  Each call clears the scratch's status word and merge counters on `stream`
+ * (cudaMemsetAsync) and allocates nothing.  All calls share the one array, so calls that
+ * may overlap on the GPU (other streams, other threads) race and must be serialised by the
+ * caller.  Device-side errors of this variant stay in the library's scratch.
+ * Errors: INVALID_ARG, MODE, WORKSPACE, CUDA. */
+msa_status_t msa_decode_no_alloc(const msa_plan_t* plan, const void* plan_dev, const void* q,
+                                 const void* k_pool, const void* v_pool,
+                                 void* out, float* lse, float scale, cudaStream_t stream);
+
 /* Merge two partial attention results over disjoint key sets (elementwise over
  * rows x heads): m = max(lse_a, lse_b), w = exp(lse - m), O = (w_a O_a + w_b O_b)/(w_a + w_b),
  * LSE = m + ln(w_a + w_b); a part with lse = -inf weighs 0; both -inf give O = 0, LSE = -inf.

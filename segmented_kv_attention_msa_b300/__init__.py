@@ -67,6 +67,7 @@ EXPORTS = {
     "msa_chunk_sizes": (_I32, [_I32, _I32, _I32, _P, _I32, _I32P]),
     "msa_prefill": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _SZ, _P]),
     "msa_decode": (_I32, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _SZ, _P]),
+    "msa_decode_no_alloc": (_I32, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P]),
     "msa_merge_lse": (_I32, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P]),
     "msa_gather": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "msa_get_status": (_I32, [_P, _P]),
