@@ -180,22 +180,30 @@ def run_ours(args, world, rank, local):
     pout = torch.empty_like(pw.q)
     plse = torch.empty(pw.q.shape[0], pw.q.shape[1], dtype=torch.float32, device=dev)
 
-    dl = W.make_layout(args.decode_workload)
-    dw = W.make_values(dl, device=dev)
-    dplan = msa.Plan.from_layout(dl).upload(dev)
-    dst = dplan.stats()
-    dout = torch.empty_like(dw.q)
-    dlse = torch.empty(dw.q.shape[0], dw.q.shape[1], dtype=torch.float32, device=dev)
+    do_pf = args.only in (None, "prefill")
+    do_dc = args.only in (None, "decode")
+    if do_dc:
+        dl = W.make_layout(args.decode_workload)
+        dw = W.make_values(dl, device=dev)
+        dplan = msa.Plan.from_layout(dl).upload(dev)
+        dst = dplan.stats()
+        dout = torch.empty_like(dw.q)
+        dlse = torch.empty(dw.q.shape[0], dw.q.shape[1], dtype=torch.float32, device=dev)
+    else:
+        dl, dw, dplan, dout, dlse = pl, None, pplan, None, None
+        dst = {"algorithmic_bytes": 0, "kv_tokens": 0, "num_splits": 0}
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MB > 126 MB L2
 
     def step(ev=None):
         if ev is not None:
             ev[0].record()
-        msa.prefill(pplan, pw.q, pw.k_chunk, pw.v_chunk, pw.k_pool, pw.v_pool, out=pout, lse=plse)
+        if do_pf:
+            msa.prefill(pplan, pw.q, pw.k_chunk, pw.v_chunk, pw.k_pool, pw.v_pool, out=pout, lse=plse)
         if ev is not None:
             ev[1].record()
-        msa.decode(dplan, dw.q, dw.k_pool, dw.v_pool, out=dout, lse=dlse)
+        if do_dc:
+            msa.decode(dplan, dw.q, dw.k_pool, dw.v_pool, out=dout, lse=dlse)
         if ev is not None:
             ev[2].record()
 
@@ -203,7 +211,7 @@ def run_ours(args, world, rank, local):
         flush.fill_(1)
         step()
     torch.cuda.synchronize()
-    if msa.get_status(pplan) != 0 or msa.get_status(dplan) != 0:
+    if msa.get_status(pplan) != 0 or (do_dc and msa.get_status(dplan) != 0):
         raise RuntimeError("device error during warm-up")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -219,13 +227,15 @@ def run_ours(args, world, rank, local):
     barrier(world)
     wall = time.perf_counter() - t0
     clocks = sampler.stop()
-    if msa.get_status(pplan) != 0 or msa.get_status(dplan) != 0:
+    if msa.get_status(pplan) != 0 or (do_dc and msa.get_status(dplan) != 0):
         raise RuntimeError("device error during the timed steps")
     pf_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)]
     dc_ms = [evs[k][1].elapsed_time(evs[k][2]) for k in range(args.steps)]
     pf_mean, dc_mean = statistics.mean(pf_ms), statistics.mean(dc_ms)
     pf_mean, dc_mean = reduce_max([pf_mean, dc_mean], world, dev)
 
+    if not (do_pf and do_dc):
+        return _single_kernel_result(args, world, pl, dl, pst, dst, pf_mean, dc_mean, peaks, peak_kind, clocks)
     flops = pst["useful_flops"]
     dbytes = dst["algorithmic_bytes"]
     value = aggregate([flops] * world, pf_mean * 1e-3) / 1e12
@@ -322,6 +332,30 @@ def run_ours(args, world, rank, local):
     return result
 
 
+def _single_kernel_result(args, world, pl, dl, pst, dst, pf_mean, dc_mean, peaks, peak_kind, clocks):
+    """Result line of a one-kernel run (--only), used for profiling captures."""
+    res = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "only": args.only,
+           "higher_is_better": True, "scaling": "weak", "dtype": "bf16", "data": "synthetic", "clocks": clocks,
+           "gpu_launches": args.steps}
+    if args.only == "prefill":
+        ach = pst["useful_flops"] / (pf_mean * 1e-3) / 1e12
+        res.update({"value": round(ach, 3), "unit": "TFLOP/s", "ms_per_step": round(pf_mean, 4),
+                    "config": {"workload": pl.name},
+                    "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
+                                 "traffic": kernel_traffic("prefill", "msa_prefill.cu"),
+                                 "peak_source": f"{peak_kind} bf16_tflops (burst)"}})
+    else:
+        ach = dst["algorithmic_bytes"] / (dc_mean * 1e-3) / 1e9
+        res.update({"value": round(ach, 1), "unit": "GB/s", "ms_per_step": round(dc_mean, 4),
+                    "config": {"workload": dl.name},
+                    "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": round(ach / peaks["hbm_gbs"], 4),
+                                 "traffic": kernel_traffic("decode", "msa_decode.cu"),
+                                 "peak_source": f"{peak_kind} hbm_gbs"}})
+    return res
+
+
 # ----------------------------------------------------------------------------- the oracle as baseline
 
 def oracle_prefill_sample(pl, arrays, rows):
@@ -416,6 +450,8 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="time one kernel alone (for profiling captures); not the bench line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
