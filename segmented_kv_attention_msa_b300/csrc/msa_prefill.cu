@@ -10,7 +10,8 @@
 //
 // How (one persistent CTA per SM, warp-specialised, 320 threads):
 //  * warp 9 (producer): TMA loads of the Q tiles (two query heads sharing one KV head,
-//    128 chunk rows each) and of each KV tile into a 2-stage ring.  A pool KV tile is 8
+//    128 chunk rows each), of each K tile into a 3-deep ring and of each V tile into a
+//    2-deep ring (a K slot frees as soon as its QK^T is done, so K runs well ahead).  A pool KV tile is 8
 //    paged blocks, one 16-row box per block and 64-column slab; a chunk KV tile is one
 //    128-row box per slab.  Missing blocks of a short pool tile are loaded from an
 //    out-of-range row and arrive as zeros.  The producer also writes each tile's 128
@@ -40,21 +41,28 @@ namespace msa {
 
 
 constexpr int kPfThreads = 320;
-constexpr int kPfStages = 2;
+constexpr int kKStages = 3;            // K tiles in flight (a slot frees once its QK^T is done)
+constexpr int kVStages = 2;            // V tiles (a slot frees once its PV is done)
 constexpr int kSlabBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 
+// Shared memory: small items first (barriers, key positions), then the operand tiles on
+// a 1024-byte boundary (the 128-byte swizzle pattern repeats every 1024 bytes).
 template <int D>
 struct PfLayout {
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kQ = 0;
+  static constexpr int kNumBars = 23;
+  static constexpr int kBar = 0;
+  static constexpr int kMisc = (kBar + kNumBars * 8 + 15) / 16 * 16;  // TMEM base address, abort flag
+  static constexpr int kPos = (kMisc + 16 + 127) / 128 * 128;          // int32 [kVStages][128], read as int4
+  static constexpr int kSmall = kPos + kVStages * 128 * 4;
+  static constexpr int kQ = 0;                         // offsets from the aligned tile base
   static constexpr int kK = kQ + 2 * kTileBytes;
-  static constexpr int kV = kK + kPfStages * kTileBytes;
-  static constexpr int kPos = kV + kPfStages * kTileBytes;
-  static constexpr int kBar = kPos + kPfStages * 128 * 4;
-  static constexpr int kNumBars = 17;
-  static constexpr int kEnd = kBar + kNumBars * 8 + 16;
-  static constexpr int kBytes = kEnd + 1024;  // slack for 1024-byte alignment of the base
+  static constexpr int kV = kK + kKStages * kTileBytes;
+  static constexpr int kTiles = kV + kVStages * kTileBytes;
+  static constexpr int kBytes = kSmall + 1023 + kTiles;
 };
+static_assert(PfLayout<128>::kBytes <= 232448, "prefill shared memory exceeds 227 KB");
+static_assert(PfLayout<128>::kPos % 16 == 0 && PfLayout<128>::kMisc % 16 == 0, "16-byte alignment");
 
 // Bounded wait that also gives up as soon as another role of this CTA gave up.
 __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, const PrefillParams& p,
@@ -82,6 +90,57 @@ __device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity, con
   return __all_sync(0xffffffffu, ok);
 }
 
+// d = a * b + c on two fp32 lanes at once (one packed FMA).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\t"
+      "mov.b64 rc, {%6,%7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0,%1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0,%1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// A KV tile record spread over a warp: lane i holds word i of the 32-word record.
+// Fields are read with warp shuffles, so every lane must take part.
+struct TileRec {
+  int v;
+  __device__ __forceinline__ int get(int i) const { return __shfl_sync(0xffffffffu, v, i); }
+};
+__device__ __forceinline__ TileRec load_tile_rec(const PrefillParams& p, const QTileRec& qt, int j, int lane) {
+  const int e = __ldg(p.list + qt.list_begin + j);
+  const int* rec = reinterpret_cast<const int*>(p.kt + (e & 0x7fffffff));
+  return TileRec{__ldg(rec + lane)};
+}
+
+// Issue the TMA loads of one K or V tile (whole warp calls; lane 0 posts the byte
+// count, lanes 0-7 load one 16-row paged block each, or lane 0 the 128-row chunk box).
+template <int D>
+__device__ __forceinline__ void issue_kv_tile(const TileRec& rec, uint8_t* dst, uint64_t* bar,
+                                              const CUtensorMap* tm_chunk, const CUtensorMap* tm_pool,
+                                              int g, int Hkv, int pool_rows, int lane) {
+  constexpr int kSlabs = D / 64;
+  const int src = rec.get(0), row0 = rec.get(2), nblk = rec.get(3);
+  const int blk = rec.get(8 + (lane & 7));
+  if (lane == 0) mbar_arrive_expect_tx(bar, 128 * D * 2);
+  __syncwarp();
+  if (src == SRC_CHUNK) {
+    if (lane == 0)
+      for (int s = 0; s < kSlabs; ++s) tma_load_2d(dst + s * kSlabBytes, tm_chunk, bar, g * D + s * 64, row0);
+  } else if (lane < kTileBlocks) {
+    // a missing block reads an out-of-range row and arrives as zeros
+    const int y = (lane < nblk) ? (blk * Hkv + g) * kBlock : pool_rows;
+    for (int s = 0; s < kSlabs; ++s) tma_load_2d(dst + s * kSlabBytes + lane * 2048, tm_pool, bar, s * 64, y);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
     msa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
@@ -94,34 +153,41 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   constexpr float kLn2 = 0.69314718055994531f;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = sm + L::kQ;
-  uint8_t* sK = sm + L::kK;
-  uint8_t* sV = sm + L::kV;
-  int32_t* sPos = reinterpret_cast<int32_t*>(sm + L::kPos);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L::kBar);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;     // [2]
-  uint64_t* v_full = bars + 4;     // [2]
-  uint64_t* kv_empty = bars + 6;   // [2]
-  uint64_t* s_full = bars + 8;     // [2] per head
-  uint64_t* p_full = bars + 10;    // [2]
-  uint64_t* o_full = bars + 12;    // [2]
-  uint64_t* o_free = bars + 14;    // [2]
-  uint64_t* drain = bars + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::kNumBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* k_full = bars + 2;     // [3]
+  uint64_t* k_empty = bars + 5;    // [3]
+  uint64_t* v_full = bars + 8;     // [2]
+  uint64_t* v_empty = bars + 10;   // [2]
+  uint64_t* pos_full = bars + 12;  // [2] key positions of the tile held in V slot s
+  uint64_t* s_full = bars + 14;    // [2] per head
+  uint64_t* p_full = bars + 16;    // [2]
+  uint64_t* o_full = bars + 18;    // [2]
+  uint64_t* o_free = bars + 20;    // [2]
+  uint64_t* drain = bars + 22;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + L::kMisc + 4);
+  int32_t* sPos = reinterpret_cast<int32_t*>(smem_raw + L::kPos);
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw + L::kSmall) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = tiles + L::kQ;
+  uint8_t* sK = tiles + L::kK;
+  uint8_t* sV = tiles + L::kV;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < kPfStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
+      mbar_init(&pos_full[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
@@ -144,14 +210,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (warp == 9) {
     // ------------------------------------------------------------ producer
-    int it = 0, wi = 0;
-    int last_it[kPfStages] = {-1, -1};
+    // Per work item: Q, K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1).  K(j) waits for
+    // the QK^T of the tile three back in its slot; V(j) waits for the PV of the tile two
+    // back, which also frees that slot's key positions (that tile's softmax is done).
+    int kit = 0, vit = 0, wi = 0;  // K tiles, V tiles and work items issued
+    int last_k[kKStages] = {-1, -1, -1};
+    int last_v[kVStages] = {-1, -1};
     int last_wi = -1;
     for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
       const WorkRec wk = p.work[w];
       const QTileRec qt = p.qt[wk.qt];
       const int n = qt.list_count;
       if (n == 0) continue;
+      TileRec cur = load_tile_rec(p, qt, 0, lane);
       if (!pf_wait_warp(q_empty, (wi & 1) ^ 1, p, abort_flag)) goto producer_done;
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, p.hpc * L::kTileBytes);
@@ -160,70 +231,60 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tma_load_2d(sQ + t * L::kTileBytes + s * kSlabBytes, &tm_q, q_full, (wk.h0 + t) * D + s * 64, qt.row0);
       }
       last_wi = wi;
-      for (int j = 0; j < n; ++j, ++it) {
-        const int st = it % kPfStages;
-        if (!pf_wait_warp(&kv_empty[st], ((it / kPfStages) & 1) ^ 1, p, abort_flag)) goto producer_done;
-        const int e = p.list[qt.list_begin + j];
-        const KTileRec* kt = p.kt + (e & 0x7fffffff);
-        const int src = kt->src, ntok = kt->ntok, row0 = kt->row0, nblk = kt->nblk;
-        for (int r = lane; r < 128; r += 32) {
-          int pos;
-          if (src == SRC_CHUNK) {
-            pos = (r < ntok) ? p.qpos[row0 + r] : 0x7fffffff;
-          } else {
+      TileRec prev = cur;
+      for (int j = 0; j <= n; ++j) {
+        TileRec nxt = cur;
+        if (j + 1 < n) nxt = load_tile_rec(p, qt, j + 1, lane);
+        if (j < n) {
+          const int ks = kit % kKStages;
+          if (!pf_wait_warp(&k_empty[ks], ((kit / kKStages) & 1) ^ 1, p, abort_flag)) goto producer_done;
+          issue_kv_tile<D>(cur, sK + ks * L::kTileBytes, &k_full[ks], &tm_kc, &tm_kp, wk.g, p.Hkv, p.pool_rows,
+                           lane);
+          last_k[ks] = kit;
+          ++kit;
+        }
+        if (j >= 1) {
+          // V and key positions of the previous tile
+          const int vs = vit % kVStages;
+          if (!pf_wait_warp(&v_empty[vs], ((vit / kVStages) & 1) ^ 1, p, abort_flag)) goto producer_done;
+          issue_kv_tile<D>(prev, sV + vs * L::kTileBytes, &v_full[vs], &tm_vc, &tm_vp, wk.g, p.Hkv, p.pool_rows,
+                           lane);
+          last_v[vs] = vit;
+          const int src = prev.get(0), ntok = prev.get(1), row0 = prev.get(2), nblk = prev.get(3);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int r = q4 * 32 + lane;
             const int i = r >> 4, tt = r & 15;
-            pos = (i < nblk && tt < kt->bfill[i]) ? kt->bpos[i] + tt : 0x7fffffff;
+            const int bp = prev.get(16 + i);
+            const int bf = prev.get(24 + i);
+            int pos;
+            if (src == SRC_CHUNK) pos = (r < ntok) ? __ldg(p.qpos + row0 + r) : 0x7fffffff;
+            else pos = (i < nblk && tt < bf) ? bp + tt : 0x7fffffff;
+            sPos[vs * 128 + r] = pos;
           }
-          sPos[st * 128 + r] = pos;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pos_full[vs]);
+          ++vit;
         }
-        __threadfence_block();
-        __syncwarp();
-        if (lane == 0) {
-          uint8_t* dK = sK + st * L::kTileBytes;
-          uint8_t* dV = sV + st * L::kTileBytes;
-          mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
-          if (src == SRC_CHUNK) {
-            for (int s = 0; s < kSlabs; ++s)
-              tma_load_2d(dK + s * kSlabBytes, &tm_kc, &k_full[st], wk.g * D + s * 64, row0);
-          } else {
-            for (int i = 0; i < kTileBlocks; ++i) {
-              const int y = (i < nblk) ? (kt->blk[i] * p.Hkv + wk.g) * kBlock : p.pool_rows;
-              for (int s = 0; s < kSlabs; ++s)
-                tma_load_2d(dK + s * kSlabBytes + i * 2048, &tm_kp, &k_full[st], s * 64, y);
-            }
-          }
-          mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
-          if (src == SRC_CHUNK) {
-            for (int s = 0; s < kSlabs; ++s)
-              tma_load_2d(dV + s * kSlabBytes, &tm_vc, &v_full[st], wk.g * D + s * 64, row0);
-          } else {
-            for (int i = 0; i < kTileBlocks; ++i) {
-              const int y = (i < nblk) ? (kt->blk[i] * p.Hkv + wk.g) * kBlock : p.pool_rows;
-              for (int s = 0; s < kSlabs; ++s)
-                tma_load_2d(dV + s * kSlabBytes + i * 2048, &tm_vp, &v_full[st], s * 64, y);
-            }
-          }
-        }
-        last_it[st] = it;
-        __syncwarp();
+        prev = cur;
+        cur = nxt;
       }
       ++wi;
     }
   producer_done:
     // every copy this warp started must land before the CTA may exit
-    for (int s = 0; s < kPfStages; ++s)
-      if (last_it[s] >= 0) {
-        mbar_wait(&k_full[s], (last_it[s] / kPfStages) & 1, 1000000000ull);
-        mbar_wait(&v_full[s], (last_it[s] / kPfStages) & 1, 1000000000ull);
-      }
+    for (int s = 0; s < kKStages; ++s)
+      if (last_k[s] >= 0) mbar_wait(&k_full[s], (last_k[s] / kKStages) & 1, 1000000000ull);
+    for (int s = 0; s < kVStages; ++s)
+      if (last_v[s] >= 0) mbar_wait(&v_full[s], (last_v[s] / kVStages) & 1, 1000000000ull);
     if (last_wi >= 0) mbar_wait(q_full, last_wi & 1, 1000000000ull);
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int it = 0, wi = 0;
-      auto issue_qk = [&](int t, int st) {
+      auto issue_qk = [&](int t, int ks) {
         const uint32_t qa = smem_u32(sQ + t * L::kTileBytes);
-        const uint32_t ka = smem_u32(sK + st * L::kTileBytes);
+        const uint32_t ka = smem_u32(sK + ks * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
@@ -231,8 +292,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                   kIdescQK, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, int st, bool acc) {
-        const uint32_t va = smem_u32(sV + st * L::kTileBytes);
+      auto issue_pv = [&](int t, int vs, bool acc) {
+        const uint32_t va = smem_u32(sV + vs * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
@@ -244,43 +305,45 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (n == 0) continue;
         if (!pf_wait(q_full, wi & 1, p, abort_flag)) goto mma_done;
         {
-          const int st0 = it % kPfStages;
-          if (!pf_wait(&k_full[st0], (it / kPfStages) & 1, p, abort_flag)) goto mma_done;
+          const int ks0 = it % kKStages;
+          if (!pf_wait(&k_full[ks0], (it / kKStages) & 1, p, abort_flag)) goto mma_done;
           tc_fence_after();
           for (int t = 0; t < p.hpc; ++t) {
-            issue_qk(t, st0);
+            issue_qk(t, ks0);
             umma_commit(&s_full[t]);
           }
+          umma_commit(&k_empty[ks0]);
           if (n == 1) umma_commit(q_empty);
         }
         for (int j = 0; j < n; ++j) {
-          const int cur = it + j, st = cur % kPfStages;
-          const int nxt = cur + 1, stn = nxt % kPfStages;
+          const int cur = it + j, vs = cur % kVStages;
+          const int nxt = cur + 1, ksn = nxt % kKStages;
           const bool has_next = j + 1 < n;
           bool have_v = false, have_kn = false;
           for (int t = 0; t < p.hpc; ++t) {
             if (!pf_wait(&p_full[t], cur & 1, p, abort_flag)) goto mma_done;
             if (j == 0 && !pf_wait(&o_free[t], (wi & 1) ^ 1, p, abort_flag)) goto mma_done;
             if (!have_v) {
-              if (!pf_wait(&v_full[st], (cur / kPfStages) & 1, p, abort_flag)) goto mma_done;
+              if (!pf_wait(&v_full[vs], (cur / kVStages) & 1, p, abort_flag)) goto mma_done;
               have_v = true;
             }
             tc_fence_after();
-            issue_pv(t, st, j > 0);
+            issue_pv(t, vs, j > 0);
             if (has_next) {
               if (!have_kn) {
-                if (!pf_wait(&k_full[stn], (nxt / kPfStages) & 1, p, abort_flag)) goto mma_done;
+                if (!pf_wait(&k_full[ksn], (nxt / kKStages) & 1, p, abort_flag)) goto mma_done;
                 have_kn = true;
                 tc_fence_after();
               }
-              issue_qk(t, stn);
+              issue_qk(t, ksn);
               umma_commit(&s_full[t]);
             } else {
               umma_commit(&o_full[t]);
             }
           }
+          if (has_next) umma_commit(&k_empty[ksn]);
           if (j + 2 == n) umma_commit(q_empty);
-          umma_commit(&kv_empty[st]);
+          umma_commit(&v_empty[vs]);
         }
         it += n;
         ++wi;
@@ -297,6 +360,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + 256 + t * 128;
+    const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
     int it = 0, wi = 0;
     for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
       const WorkRec wk = p.work[w];
@@ -310,11 +374,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       const int h = wk.h0 + t;
       const bool valid = r < qt.nrows;
-      const int qp = valid ? p.qpos[qt.row0 + r] : -1;
+      const int qp = valid ? __ldg(p.qpos + qt.row0 + r) : -1;
       float m_used = -INFINITY, l = 0.f;
+      int e_next = __ldg(p.list + qt.list_begin);
       for (int j = 0; j < n; ++j, ++it) {
-        const int st = it % kPfStages;
-        const bool partial = p.list[qt.list_begin + j] < 0;
+        const int vs = it % kVStages;
+        const bool partial = e_next < 0;
+        if (j + 1 < n) e_next = __ldg(p.list + qt.list_begin + j + 1);
         if (!pf_wait_warp(&s_full[t], it & 1, p, abort_flag)) goto softmax_done;
         tc_fence_after();
         uint32_t s[128];
@@ -324,8 +390,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_ld_x32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
         tmem_wait_ld();
         if (partial) {
-          if (!pf_wait_warp(&k_full[st], (it / kPfStages) & 1, p, abort_flag)) goto softmax_done;
-          const int4* kp4 = reinterpret_cast<const int4*>(sPos + st * 128);
+          if (!pf_wait_warp(&pos_full[vs], (it / kVStages) & 1, p, abort_flag)) goto softmax_done;
+          const int4* kp4 = reinterpret_cast<const int4*>(sPos + vs * 128);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int4 kp = kp4[c];
@@ -335,9 +401,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (kp.w > qp) s[4 * c + 3] = __float_as_uint(-INFINITY);
           }
         }
-        float mx = -INFINITY;
+        // row max: eight independent chains, then a tree
+        float m8[8];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(s[i]);
+#pragma unroll
+        for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(s[c]));
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         const float m_cand = mx * p.scale_log2;
         const bool need = m_cand > m_used + 8.f;
         const bool resc = need && (m_used != -INFINITY);
@@ -360,15 +431,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           tmem_wait_st();
         }
         const float ms = (m_used == -INFINITY) ? 0.f : m_used;
-        float rowsum = 0.f;
+        const float2 nms2 = make_float2(-ms, -ms);
+        float2 acc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(s[2 * c]), p.scale_log2, -ms));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(s[2 * c + 1]), p.scale_log2, -ms));
-          rowsum += p0 + p1;
-          s[c] = pack_bf16x2(p0, p1);
+          const float2 x =
+              ffma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), scale2, nms2);
+          const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          acc[c & 3] = fadd2(acc[c & 3], pe);
+          s[c] = pack_bf16x2(pe.x, pe.y);
         }
-        l += rowsum;
+        const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+        l += a.x + a.y;
         tmem_st_x32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
         tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_wait_st();
