@@ -70,7 +70,9 @@ typedef struct {
   int32_t block_size;         /* tokens per pool block, must be 16 */
   int32_t decode_split_blocks;/* decode: pool blocks per split-KV work unit, 0 = automatic */
   int32_t decode_min_ctas;    /* decode: target number of CTAs when automatic, 0 = 16 x SMs */
-  int32_t reserved[4];        /* must be 0 */
+  int32_t prefill_ctas;       /* prefill: CTAs of the persistent launch the work is balanced
+                                 over (one per SM), 0 = 148 (the B300's SM count) */
+  int32_t reserved[3];        /* must be 0 */
 } msa_plan_opts_t;
 
 typedef struct msa_plan msa_plan_t;
@@ -85,6 +87,8 @@ typedef struct {
   int32_t num_tile_pairs;     /* prefill: non-skipped (query tile, KV tile) pairs x heads/2 */
   int32_t num_partial_pairs;
   int32_t num_splits;         /* decode split units (before x Hkv) */
+  int32_t num_prefill_ctas;   /* prefill: CTAs of the launch */
+  int32_t num_split_items;    /* prefill: work items cut into several pieces (merged on device) */
 } msa_plan_stats_t;
 
 /* Build a plan on the host (no CUDA call).  Inputs are host arrays, copied.
@@ -113,7 +117,8 @@ void msa_plan_destroy(msa_plan_t* plan);
 size_t msa_plan_device_bytes(const msa_plan_t* plan);
 msa_status_t msa_plan_upload(const msa_plan_t* plan, void* plan_dev, size_t bytes, cudaStream_t stream);
 
-/* Workspace: status word, scheduling counters and (decode) split partials.  The caller
+/* Workspace: status word, merge counters and partial results (decode split-KV units;
+ * prefill work items cut into pieces).  The caller
  * allocates msa_workspace_bytes (256-byte aligned) and calls msa_workspace_init once
  * before first use (it zeroes the buffer on `stream`); the kernels leave it re-usable.
  * A workspace must not be shared by launches that may overlap. */
@@ -136,6 +141,14 @@ msa_status_t msa_plan_export(const msa_plan_t* plan, int32_t* out, size_t capaci
 
 /* Decode split units as int32 triples (seq, first canonical block, number of blocks). */
 msa_status_t msa_plan_export_splits(const msa_plan_t* plan, int32_t* out, size_t capacity, size_t* n);
+
+/* Prefill schedule as int32 records of 9 words, one per piece, grouped by CTA in the
+ * order each CTA runs them: (cta, query tile, KV head, first query head, first list entry,
+ * list entries, pieces of the work item, first partial slot of the item, own slot).  The
+ * list of a query tile is its non-skipped KV tiles, full ones first, each group in
+ * position order.  A work item is (query tile, KV head, first query head); its pieces
+ * cover its list exactly once.  Decode plans export nothing. */
+msa_status_t msa_plan_export_schedule(const msa_plan_t* plan, int32_t* out, size_t capacity, size_t* n);
 
 msa_status_t msa_plan_get_stats(const msa_plan_t* plan, msa_plan_stats_t* stats);
 
@@ -211,9 +224,10 @@ msa_status_t msa_gather(const msa_plan_t* plan, const void* plan_dev,
  * the device-side error (e.g. MSA_ERR_TIMEOUT). */
 msa_status_t msa_get_status(void* workspace, cudaStream_t stream);
 
-/* Device-wait bound (spin iterations of each mbarrier wait before giving up with
- * MSA_ERR_TIMEOUT); 0 restores the default.  Applies to later launches. */
-void msa_set_wait_limit(int64_t spins);
+/* Device-wait bound: nanoseconds (global timer) that each mbarrier wait of a kernel may
+ * spin before the kernel gives up with MSA_ERR_TIMEOUT; <= 0 restores the default of
+ * 2 s.  Applies to later launches. */
+void msa_set_wait_limit(int64_t ns);
 
 const char* msa_status_string(msa_status_t status);
 int32_t msa_version(void);

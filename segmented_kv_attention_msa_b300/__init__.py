@@ -35,7 +35,7 @@ class _Opts(ctypes.Structure):
     _fields_ = [("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("decode_split_blocks", ctypes.c_int32), ("decode_min_ctas", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 4)]
+                ("prefill_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 class _Stats(ctypes.Structure):
@@ -43,7 +43,8 @@ class _Stats(ctypes.Structure):
                 ("algorithmic_bytes", ctypes.c_int64), ("num_kv_tiles", ctypes.c_int32),
                 ("num_q_tiles", ctypes.c_int32), ("num_work_items", ctypes.c_int32),
                 ("num_tile_pairs", ctypes.c_int32), ("num_partial_pairs", ctypes.c_int32),
-                ("num_splits", ctypes.c_int32)]
+                ("num_splits", ctypes.c_int32), ("num_prefill_ctas", ctypes.c_int32),
+                ("num_split_items", ctypes.c_int32)]
 
 
 _lib = None
@@ -63,6 +64,7 @@ EXPORTS = {
     "msa_workspace_init": (_I32, [_P, _SZ, _P]),
     "msa_plan_export": (_I32, [_P, _P, _SZ, ctypes.POINTER(_SZ)]),
     "msa_plan_export_splits": (_I32, [_P, _P, _SZ, ctypes.POINTER(_SZ)]),
+    "msa_plan_export_schedule": (_I32, [_P, _P, _SZ, ctypes.POINTER(_SZ)]),
     "msa_plan_get_stats": (_I32, [_P, ctypes.POINTER(_Stats)]),
     "msa_chunk_sizes": (_I32, [_I32, _I32, _I32, _P, _I32, _I32P]),
     "msa_prefill": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _SZ, _P]),
@@ -127,10 +129,11 @@ class Plan:
 
     def __init__(self, mode: str, num_heads_q: int, num_heads_kv: int, head_dim: int,
                  segments, block_table, block_pos, block_fill, cu_q, q_pos=None,
-                 decode_split_blocks: int = 0, decode_min_ctas: int = 0):
+                 decode_split_blocks: int = 0, decode_min_ctas: int = 0, prefill_ctas: int = 0):
         self.mode = mode
         m = MSA_PREFILL if mode == "prefill" else MSA_DECODE
-        opts = _Opts(num_heads_q, num_heads_kv, head_dim, 16, decode_split_blocks, decode_min_ctas)
+        opts = _Opts(num_heads_q, num_heads_kv, head_dim, 16, decode_split_blocks, decode_min_ctas,
+                     prefill_ctas)
         self._keep = [np.ascontiguousarray(np.asarray(x, np.int32)) for x in
                       (segments, block_table, block_pos, block_fill, cu_q,
                        q_pos if q_pos is not None else np.zeros(0, np.int32))]
@@ -186,6 +189,15 @@ class Plan:
         _check(lib().msa_plan_export_splits(self._h, _ptr(out), n.value, ctypes.byref(n)),
                "msa_plan_export_splits")
         return out[:n.value].reshape(-1, 3)
+
+    def export_schedule(self) -> np.ndarray:
+        """Prefill pieces, one row each: (cta, qt, g, h0, j0, n, nparts, slot0, slot)."""
+        n = ctypes.c_size_t(0)
+        _check(lib().msa_plan_export_schedule(self._h, None, 0, ctypes.byref(n)), "msa_plan_export_schedule")
+        out = np.zeros(max(1, n.value), np.int32)
+        _check(lib().msa_plan_export_schedule(self._h, _ptr(out), n.value, ctypes.byref(n)),
+               "msa_plan_export_schedule")
+        return out[:n.value].reshape(-1, 9)
 
     def stats(self) -> dict:
         s = _Stats()

@@ -71,10 +71,15 @@ extern "C" msa_status_t msa_prefill(const msa_plan_t* plan, const void* plan_dev
   p.kt = at<KTileRec>(plan_dev, plan->dev.ktile);
   p.list = at<int32_t>(plan_dev, plan->dev.list);
   p.work = at<WorkRec>(plan_dev, plan->dev.work);
+  p.cta_begin = at<int32_t>(plan_dev, plan->dev.cta);
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
-  p.status = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) + plan->ws.status);
-  p.n_work = plan->n_work;
+  char* ws = reinterpret_cast<char*>(workspace);
+  p.part_o = reinterpret_cast<float4*>(ws + plan->ws.pf_part_o);
+  p.part_ml = reinterpret_cast<float2*>(ws + plan->ws.pf_part_ml);
+  p.counters = reinterpret_cast<int32_t*>(ws + plan->ws.pf_counters);
+  p.status = reinterpret_cast<int32_t*>(ws + plan->ws.status);
+  p.n_ctas = plan->n_ctas;
   p.Hq = plan->Hq;
   p.Hkv = plan->Hkv;
   p.hpc = plan->hpc;

@@ -35,9 +35,13 @@ struct KTileRec {
   int32_t bfill[kTileBlocks];
 };
 
-// One prefill CTA work item: query tile `qt`, KV head `g`, query heads h0 .. h0+hpc-1.
+// One piece of prefill work: query tile `qt`, KV head `g`, query heads h0 .. h0+hpc-1,
+// over entries [j0, j0 + n) of the query tile's KV-tile list.  A work item (qt, g, h0)
+// whose list is cut into nparts > 1 pieces (to balance the CTAs) writes one partial
+// result per piece into workspace slot `slot` (slot0 .. slot0 + nparts - 1); the piece
+// that finishes last (counter `slot0`) merges them.  nparts == 1: written directly.
 struct WorkRec {
-  int32_t qt, g, h0, cost;
+  int32_t qt, g, h0, j0, n, nparts, slot0, slot;
 };
 
 // One decode split-KV unit: canonical blocks [blk_begin, blk_begin + blk_count) of the
@@ -55,12 +59,12 @@ struct GatherRec {
 
 // Byte offsets of each section within the device image.
 struct DevLayout {
-  size_t qpos, qtile, ktile, list, work, split, blist, bfill, gather, total;
+  size_t qpos, qtile, ktile, list, work, cta, split, blist, bfill, gather, total;
 };
 
 // Byte offsets within the workspace.
 struct WsLayout {
-  size_t status, counters, part_o, part_lse, total;
+  size_t status, counters, part_o, part_lse, pf_counters, pf_part_o, pf_part_ml, total;
 };
 
 }  // namespace msa
@@ -70,8 +74,10 @@ struct msa_plan {
   msa_mode_t mode;
   int32_t num_seqs, Hq, Hkv, d, G, hpc, num_pool_blocks;
   int32_t total_q, n_tok, n_qt, n_kt, n_list, n_work, n_split, n_blist, n_gather;
+  int32_t n_ctas, n_slots;          // prefill: CTAs of the launch, partial-result slots
   std::vector<int32_t> canon;       // canonical export
   std::vector<int32_t> split_export;
+  std::vector<int32_t> sched_export;
   std::vector<int32_t> image;       // device image (int32 words)
   msa::DevLayout dev;
   msa::WsLayout ws;

@@ -13,10 +13,14 @@ struct PrefillParams {
   const KTileRec* kt;
   const int32_t* list;
   const WorkRec* work;
+  const int32_t* cta_begin;  // pieces of CTA c: work[cta_begin[c] .. cta_begin[c + 1])
   __nv_bfloat16* out;
   float* lse;
+  float4* part_o;            // split items: unnormalised O per (slot, head), [d/4][128] float4
+  float2* part_ml;           // split items: (max in log2 units, sum) per (slot, head, row)
+  int32_t* counters;         // split items: pieces finished per (first slot, head)
   int32_t* status;
-  int32_t n_work, Hq, Hkv, hpc;
+  int32_t n_ctas, Hq, Hkv, hpc;
   int32_t pool_rows;  // rows of the pool tensor maps; a box starting here reads zeros
   float scale_log2;
   uint64_t wait_ns;

@@ -86,6 +86,128 @@ struct KTileHost {
   int32_t first_unit;
 };
 
+
+// ---------------------------------------------------------------- prefill schedule
+//
+// The prefill kernel is persistent: one CTA per SM walks a fixed list of pieces.  A work
+// item is (query tile, KV head, pair of query heads) over the query tile's list of
+// non-skipped KV tiles.  Items differ a lot in length (a query tile late in position sees
+// many more keys), and a few hundred of them over 148 SMs balance poorly when each item
+// stays whole.  So the items, longest first, are laid end to end and cut into `ctas`
+// consecutive stretches of near-equal cost; an item that straddles a cut becomes several
+// pieces, each computing a partial (O, max, sum) over its part of the list, merged on the
+// device by the piece that finishes last (log-sum-exp merge).  The cost model counts a
+// full tile as kWFull, a partial (masked) tile as kWPartial and each piece's set-up and
+// epilogue as kWPiece; no piece is shorter than kMinPiece tiles.  The smallest stretch
+// cost for which the walk fits in `ctas` CTAs is found by bisection.
+constexpr int32_t kDefaultCtas = 148;
+constexpr int64_t kWFull = 8, kWPartial = 10, kWPiece = 8;
+constexpr int32_t kMinPiece = 4;
+
+struct ItemRef {
+  int32_t qt, g, h0;
+};
+
+struct Cut {
+  int32_t item, j0, n, cta;
+};
+
+// Walk the items with stretch cost T; returns false if more than `ctas` CTAs are needed.
+bool walk_items(const std::vector<std::vector<int64_t>>& pre, const std::vector<int32_t>& order,
+                int64_t T, int32_t ctas, std::vector<Cut>* cuts) {
+  int32_t c = 0;
+  int64_t cap = T;
+  if (cuts) cuts->clear();
+  for (int32_t it : order) {
+    const std::vector<int64_t>& w = pre[it];  // prefix sums of tile weights, w[0] = 0
+    const int32_t n = (int32_t)w.size() - 1;
+    int32_t j = 0;  // an empty list (a query tile that sees nothing) makes no piece
+    while (j < n) {
+      const int64_t rest = w[n] - w[j] + kWPiece;
+      if (rest <= cap) {
+        if (cuts) cuts->push_back({it, j, n - j, c});
+        cap -= rest;
+        j = n;
+        break;
+      }
+      // longest prefix of the rest that fits in what is left of this CTA
+      int32_t j2 = j;
+      while (j2 < n && w[j2 + 1] - w[j] + kWPiece <= cap) ++j2;
+      if (n - j2 < kMinPiece) j2 = n - kMinPiece;
+      if (j2 - j >= kMinPiece) {
+        if (cuts) cuts->push_back({it, j, j2 - j, c});
+        j = j2;
+      }
+      if (++c >= ctas) return false;
+      cap = T;
+    }
+  }
+  return true;
+}
+
+void schedule_prefill(const std::vector<QTileRec>& qts, const std::vector<int32_t>& list,
+                      const std::vector<ItemRef>& items, int32_t ctas, std::vector<WorkRec>& work,
+                      std::vector<int32_t>& cta_begin, std::vector<int32_t>& sched) {
+  work.clear();
+  cta_begin.assign(1, 0);
+  sched.clear();
+  if (items.empty()) return;
+  std::vector<std::vector<int64_t>> pre(items.size());
+  int64_t total = 0;
+  for (size_t i = 0; i < items.size(); ++i) {
+    const QTileRec& q = qts[items[i].qt];
+    std::vector<int64_t>& w = pre[i];
+    w.assign(q.list_count + 1, 0);
+    for (int32_t j = 0; j < q.list_count; ++j)
+      w[j + 1] = w[j] + (list[q.list_begin + j] < 0 ? kWPartial : kWFull);
+    total += w.back() + kWPiece;
+  }
+  // longest first; ties keep (query tile, KV head, head) order
+  std::vector<int32_t> order(items.size());
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t a, int32_t b) { return pre[a].back() > pre[b].back(); });
+  ctas = std::max<int32_t>(1, ctas);
+  // with T = total everything fits in one CTA, so the bisection always ends feasible
+  int64_t lo = (total + ctas - 1) / ctas, hi = total;
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (walk_items(pre, order, mid, ctas, nullptr)) hi = mid;
+    else lo = mid + 1;
+  }
+  std::vector<Cut> cuts;
+  walk_items(pre, order, lo, ctas, &cuts);
+  // pieces per item, partial slots for items in several pieces
+  std::vector<int32_t> nparts(items.size(), 0), slot0(items.size(), -1), seen(items.size(), 0);
+  for (const Cut& c : cuts) ++nparts[c.item];
+  int32_t slots = 0;
+  for (int32_t it : order)
+    if (nparts[it] > 1) {
+      slot0[it] = slots;
+      slots += nparts[it];
+    }
+  const int32_t used = cuts.empty() ? 0 : cuts.back().cta + 1;
+  // within a CTA, pieces of split items run first (their merges then happen early),
+  // then whole items, each group in walk order
+  for (int32_t c = 0, k = 0; c < used; ++c) {
+    int32_t k1 = k;
+    while (k1 < (int32_t)cuts.size() && cuts[k1].cta == c) ++k1;
+    for (int pass = 0; pass < 2; ++pass)
+      for (int32_t i = k; i < k1; ++i) {
+        const Cut& cu = cuts[i];
+        const bool split = nparts[cu.item] > 1;
+        if ((pass == 0) != split) continue;
+        const ItemRef& r = items[cu.item];
+        const int32_t slot = split ? slot0[cu.item] + seen[cu.item]++ : -1;
+        work.push_back({r.qt, r.g, r.h0, cu.j0, cu.n, nparts[cu.item], slot0[cu.item], slot});
+        const int32_t rec[9] = {c, r.qt, r.g, r.h0, cu.j0, cu.n, nparts[cu.item], slot0[cu.item], slot};
+        sched.insert(sched.end(), rec, rec + 9);
+      }
+    cta_begin.push_back((int32_t)work.size());
+    k = k1;
+  }
+}
+
 }  // namespace
 
 extern "C" msa_status_t msa_chunk_sizes(int32_t R, int32_t min_chunk, int32_t max_chunk,
@@ -126,8 +248,9 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
     return MSA_ERR_INVALID_ARG;
   if (mode != MSA_PREFILL && mode != MSA_DECODE) return MSA_ERR_INVALID_ARG;
   if (num_segs > 0 && (!segs || !block_table || !block_pos || !block_fill)) return MSA_ERR_INVALID_ARG;
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 3; ++i)
     if (opts->reserved[i] != 0) return MSA_ERR_INVALID_ARG;
+  if (opts->prefill_ctas < 0) return MSA_ERR_INVALID_ARG;
   const int32_t Hq = opts->num_heads_q, Hkv = opts->num_heads_kv, d = opts->head_dim;
   if (Hq <= 0 || Hkv <= 0) return MSA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || (d != 64 && d != 128) || opts->block_size != kBlock) return MSA_ERR_UNSUPPORTED;
@@ -249,7 +372,9 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
 
   // ---- device image
   std::vector<int32_t> list;
+  std::vector<ItemRef> items;
   std::vector<WorkRec> work;
+  std::vector<int32_t> cta_begin{0}, sched;
   std::vector<KTileRec> ktr(kts.size());
   std::vector<SplitRec> splits;
   std::vector<int32_t> blist, bfill;
@@ -284,7 +409,6 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
       QTileRec& q = qts[qi];
       q.list_begin = (int32_t)list.size();
       int32_t s = q.seq;
-      int32_t cost = 0;
       // full tiles first, then partial ones, each group in position order
       for (int pass = 0; pass < 2; ++pass) {
         for (int32_t k = seq_kt_begin[s]; k < seq_kt_begin[s + 1]; ++k) {
@@ -294,21 +418,25 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
         }
       }
       for (int32_t k = seq_kt_begin[s]; k < seq_kt_begin[s + 1]; ++k) {
-        int32_t c = cls[ci + (k - seq_kt_begin[s])];
-        if (c != CLS_SKIP) ++cost;
-        if (c == CLS_PARTIAL) ++partial_pairs;
+        if (cls[ci + (k - seq_kt_begin[s])] == CLS_PARTIAL) ++partial_pairs;
       }
       ci += seq_kt_begin[s + 1] - seq_kt_begin[s];
       q.list_count = (int32_t)list.size() - q.list_begin;
       tile_pairs += q.list_count;
       for (int32_t g = 0; g < Hkv; ++g)
-        for (int32_t h = 0; h < P->G; h += P->hpc)
-          work.push_back({(int32_t)qi, g, g * P->G + h, cost});
+        for (int32_t h = 0; h < P->G; h += P->hpc) items.push_back({(int32_t)qi, g, g * P->G + h});
     }
-    // longest first; ties keep (qt, g, h0) order
-    std::stable_sort(work.begin(), work.end(),
-                     [](const WorkRec& a, const WorkRec& b) { return a.cost > b.cost; });
+    const int32_t ctas = opts->prefill_ctas > 0 ? opts->prefill_ctas : kDefaultCtas;
+    schedule_prefill(qts, list, items, ctas, work, cta_begin, sched);
+    P->n_ctas = (int32_t)cta_begin.size() - 1;
+    P->n_slots = 0;
+    for (const WorkRec& w : work)
+      if (w.nparts > 1) P->n_slots = std::max(P->n_slots, w.slot + 1);
+    P->sched_export = sched;
     P->stats.num_work_items = (int32_t)work.size();
+    P->stats.num_prefill_ctas = P->n_ctas;
+    for (const WorkRec& w : work)
+      if (w.nparts > 1 && w.slot == w.slot0) ++P->stats.num_split_items;
     P->stats.num_tile_pairs = (int32_t)(tile_pairs * (Hq / P->hpc));
     P->stats.num_partial_pairs = (int32_t)(partial_pairs * (Hq / P->hpc));
     int64_t bytes = 0;
@@ -407,6 +535,7 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
   L.ktile = take(ktr.size() * sizeof(KTileRec));
   L.list = take(list.size() * 4);
   L.work = take(work.size() * sizeof(WorkRec));
+  L.cta = take(cta_begin.size() * 4);
   L.split = take(splits.size() * sizeof(SplitRec));
   L.blist = take(blist.size() * 4);
   L.bfill = take(bfill.size() * 4);
@@ -422,6 +551,7 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
   put(L.ktile, ktr.data(), ktr.size() * sizeof(KTileRec));
   put(L.list, list.data(), list.size() * 4);
   put(L.work, work.data(), work.size() * sizeof(WorkRec));
+  put(L.cta, cta_begin.data(), cta_begin.size() * 4);
   put(L.split, splits.data(), splits.size() * sizeof(SplitRec));
   put(L.blist, blist.data(), blist.size() * 4);
   put(L.bfill, bfill.data(), bfill.size() * 4);
@@ -438,6 +568,14 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
   wo = align_up(wo + (size_t)P->n_split * Hq * d * 4, 256);
   W.part_lse = wo;
   wo = align_up(wo + (size_t)P->n_split * Hq * 4, 256);
+  // prefill: one merge counter per (split item, head of the pair), then per partial slot
+  // and head the unnormalised O (fp32, d/4 x 128 rows of float4) and (max, sum) per row
+  W.pf_counters = wo;
+  wo = align_up(wo + (size_t)P->n_slots * P->hpc * 4, 256);
+  W.pf_part_o = wo;
+  wo = align_up(wo + (size_t)P->n_slots * P->hpc * kTileRows * d * 4, 256);
+  W.pf_part_ml = wo;
+  wo = align_up(wo + (size_t)P->n_slots * P->hpc * kTileRows * 8, 256);
   W.total = wo;
   P->ws = W;
 
@@ -468,6 +606,16 @@ extern "C" msa_status_t msa_plan_export_splits(const msa_plan_t* plan, int32_t* 
   if (!out) return MSA_OK;
   if (capacity < plan->split_export.size()) return MSA_ERR_WORKSPACE;
   std::copy(plan->split_export.begin(), plan->split_export.end(), out);
+  return MSA_OK;
+}
+
+extern "C" msa_status_t msa_plan_export_schedule(const msa_plan_t* plan, int32_t* out,
+                                                 size_t capacity, size_t* n) {
+  if (!plan || !n) return MSA_ERR_INVALID_ARG;
+  *n = plan->sched_export.size();
+  if (!out) return MSA_OK;
+  if (capacity < plan->sched_export.size()) return MSA_ERR_WORKSPACE;
+  std::copy(plan->sched_export.begin(), plan->sched_export.end(), out);
   return MSA_OK;
 }
 

@@ -50,7 +50,7 @@ constexpr int kSlabBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 template <int D>
 struct PfLayout {
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kNumBars = 23;
+  static constexpr int kNumBars = 27;
   static constexpr int kBar = 0;
   static constexpr int kMisc = (kBar + kNumBars * 8 + 15) / 16 * 16;  // TMEM base address, abort flag
   static constexpr int kPos = (kMisc + 16 + 127) / 128 * 128;          // int32 [kVStages][128], read as int4
@@ -114,8 +114,8 @@ struct TileRec {
   int v;
   __device__ __forceinline__ int get(int i) const { return __shfl_sync(0xffffffffu, v, i); }
 };
-__device__ __forceinline__ TileRec load_tile_rec(const PrefillParams& p, const QTileRec& qt, int j, int lane) {
-  const int e = __ldg(p.list + qt.list_begin + j);
+__device__ __forceinline__ TileRec load_tile_rec(const PrefillParams& p, const int* lst, int j, int lane) {
+  const int e = __ldg(lst + j);
   const int* rec = reinterpret_cast<const int*>(p.kt + (e & 0x7fffffff));
   return TileRec{__ldg(rec + lane)};
 }
@@ -166,8 +166,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* o_full = bars + 18;    // [2]
   uint64_t* o_free = bars + 20;    // [2]
   uint64_t* drain = bars + 22;
+  uint64_t* ep_bar = bars + 23;    // [2] split pieces: the head's 128 threads stored their partial
+  uint64_t* ep_flag = bars + 25;   // [2] split pieces: merge counter read, last_flag[t] valid
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + L::kMisc + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem_raw + L::kMisc + 8);  // [2]
   int32_t* sPos = reinterpret_cast<int32_t*>(smem_raw + L::kPos);
   uint8_t* tiles = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw + L::kSmall) + 1023) & ~uintptr_t(1023));
@@ -196,6 +199,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&o_free[t], 128);
     }
     mbar_init(drain, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&ep_bar[t], 128);
+      mbar_init(&ep_flag[t], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -217,12 +224,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     int last_k[kKStages] = {-1, -1, -1};
     int last_v[kVStages] = {-1, -1};
     int last_wi = -1;
-    for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
+    for (int w = __ldg(p.cta_begin + blockIdx.x), w1 = __ldg(p.cta_begin + blockIdx.x + 1); w < w1; ++w) {
       const WorkRec wk = p.work[w];
       const QTileRec qt = p.qt[wk.qt];
-      const int n = qt.list_count;
+      const int n = wk.n;
       if (n == 0) continue;
-      TileRec cur = load_tile_rec(p, qt, 0, lane);
+      const int* lst = p.list + qt.list_begin + wk.j0;
+      TileRec cur = load_tile_rec(p, lst, 0, lane);
       if (!pf_wait_warp(q_empty, (wi & 1) ^ 1, p, abort_flag)) goto producer_done;
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, p.hpc * L::kTileBytes);
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       TileRec prev = cur;
       for (int j = 0; j <= n; ++j) {
         TileRec nxt = cur;
-        if (j + 1 < n) nxt = load_tile_rec(p, qt, j + 1, lane);
+        if (j + 1 < n) nxt = load_tile_rec(p, lst, j + 1, lane);
         if (j < n) {
           const int ks = kit % kKStages;
           if (!pf_wait_warp(&k_empty[ks], ((kit / kKStages) & 1) ^ 1, p, abort_flag)) goto producer_done;
@@ -299,9 +307,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
                   smem_desc_sw128(va + kk * 2048, kSlabBytes, 1024), kIdescPV, (acc || kk > 0) ? 1u : 0u);
       };
-      for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
-        const WorkRec wk = p.work[w];
-        const int n = p.qt[wk.qt].list_count;
+      for (int w = __ldg(p.cta_begin + blockIdx.x), w1 = __ldg(p.cta_begin + blockIdx.x + 1); w < w1; ++w) {
+        const int n = p.work[w].n;
         if (n == 0) continue;
         if (!pf_wait(q_full, wi & 1, p, abort_flag)) goto mma_done;
         {
@@ -361,11 +368,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + 256 + t * 128;
     const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
-    int it = 0, wi = 0;
-    for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
+    int it = 0, wi = 0, se = 0;  // tiles, pieces and split pieces done
+    for (int w = __ldg(p.cta_begin + blockIdx.x), w1 = __ldg(p.cta_begin + blockIdx.x + 1); w < w1; ++w) {
       const WorkRec wk = p.work[w];
       const QTileRec qt = p.qt[wk.qt];
-      const int n = qt.list_count;
+      const int n = wk.n;
       if (n == 0) continue;
       if (t >= p.hpc) {
         it += n;
@@ -376,11 +383,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const bool valid = r < qt.nrows;
       const int qp = valid ? __ldg(p.qpos + qt.row0 + r) : -1;
       float m_used = -INFINITY, l = 0.f;
-      int e_next = __ldg(p.list + qt.list_begin);
+      const int* lst = p.list + qt.list_begin + wk.j0;
+      int e_next = __ldg(lst);
       for (int j = 0; j < n; ++j, ++it) {
         const int vs = it % kVStages;
         const bool partial = e_next < 0;
-        if (j + 1 < n) e_next = __ldg(p.list + qt.list_begin + j + 1);
+        if (j + 1 < n) e_next = __ldg(lst + j + 1);
         if (!pf_wait_warp(&s_full[t], it & 1, p, abort_flag)) goto softmax_done;
         tc_fence_after();
         uint32_t s[128];
@@ -454,7 +462,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // epilogue: O / l -> bf16, LSE = ln 2 * (m + log2 l)
       if (!pf_wait_warp(&o_full[t], wi & 1, p, abort_flag)) goto softmax_done;
       tc_fence_after();
-      {
+      if (wk.nparts == 1) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const size_t orow = ((size_t)(qt.row0 + r) * p.Hq + h) * D;
 #pragma unroll 1
@@ -476,9 +484,78 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
         if (valid) p.lse[(size_t)(qt.row0 + r) * p.Hq + h] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+        tc_fence_before();
+        mbar_arrive(&o_free[t]);
+      } else {
+        // one piece of a split work item: store the unnormalised partial (O, max, sum);
+        // the piece that finishes last merges all of them in slot order (log-sum-exp
+        // merge), so the result does not depend on which piece that is.
+        const size_t sb = (size_t)wk.slot * p.hpc + t;
+        float4* po = p.part_o + sb * (D / 4) * 128;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tmem_ld_x32(tO + c, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            po[(size_t)(c / 4 + i) * 128 + r] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                                                            __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+        }
+        p.part_ml[sb * 128 + r] = make_float2(m_used, l);
+        tc_fence_before();
+        mbar_arrive(&o_free[t]);
+        // publish the partial device-wide, then one thread bumps the item's counter; the
+        // handshake inside the CTA uses bounded mbarrier waits
+        __threadfence();
+        mbar_arrive(&ep_bar[t]);
+        int32_t* counter = p.counters + (size_t)wk.slot0 * p.hpc + t;
+        if (r == 0) {
+          if (!pf_wait(&ep_bar[t], se & 1, p, abort_flag)) goto softmax_done;
+          last_flag[t] = (atomicAdd(counter, 1) == wk.nparts - 1) ? 1 : 0;
+          mbar_arrive(&ep_flag[t]);
+        }
+        if (!pf_wait_warp(&ep_flag[t], se & 1, p, abort_flag)) goto softmax_done;
+        ++se;
+        if (last_flag[t]) {
+          __threadfence();
+          const size_t s0 = (size_t)wk.slot0 * p.hpc + t;
+          float mx = -INFINITY;
+          for (int k = 0; k < wk.nparts; ++k) mx = fmaxf(mx, __ldcg(p.part_ml + (s0 + (size_t)k * p.hpc) * 128 + r).x);
+          float den = 0.f;
+          for (int k = 0; k < wk.nparts; ++k) {
+            const float2 ml = __ldcg(p.part_ml + (s0 + (size_t)k * p.hpc) * 128 + r);
+            den += (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - mx) * ml.y;
+          }
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+          if (valid) {
+            const size_t orow = ((size_t)(qt.row0 + r) * p.Hq + h) * D;
+#pragma unroll 1
+            for (int c4 = 0; c4 < D / 4; c4 += 2) {
+              float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+              for (int k = 0; k < wk.nparts; ++k) {
+                const size_t sk = s0 + (size_t)k * p.hpc;
+                const float mk = __ldcg(p.part_ml + sk * 128 + r).x;
+                const float wgt = (mk == -INFINITY) ? 0.f : fast_exp2(mk - mx);
+                const float4* pk = p.part_o + sk * (D / 4) * 128;
+                const float4 x0 = __ldcg(pk + (size_t)c4 * 128 + r), x1 = __ldcg(pk + (size_t)(c4 + 1) * 128 + r);
+                a0.x = fmaf(wgt, x0.x, a0.x); a0.y = fmaf(wgt, x0.y, a0.y);
+                a0.z = fmaf(wgt, x0.z, a0.z); a0.w = fmaf(wgt, x0.w, a0.w);
+                a1.x = fmaf(wgt, x1.x, a1.x); a1.y = fmaf(wgt, x1.y, a1.y);
+                a1.z = fmaf(wgt, x1.z, a1.z); a1.w = fmaf(wgt, x1.w, a1.w);
+              }
+              uint4 v;
+              v.x = pack_bf16x2(a0.x * inv, a0.y * inv);
+              v.y = pack_bf16x2(a0.z * inv, a0.w * inv);
+              v.z = pack_bf16x2(a1.x * inv, a1.y * inv);
+              v.w = pack_bf16x2(a1.z * inv, a1.w * inv);
+              *reinterpret_cast<uint4*>(p.out + orow + c4 * 4) = v;
+            }
+            p.lse[(size_t)(qt.row0 + r) * p.Hq + h] = den > 0.f ? (mx + __log2f(den)) * kLn2 : -INFINITY;
+          }
+          if (r == 0) *counter = 0;  // re-arm for the next launch
+        }
       }
-      tc_fence_before();
-      mbar_arrive(&o_free[t]);
       ++wi;
     }
   softmax_done:;
@@ -525,17 +602,6 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t r
 }
 
 
-static int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 template <int D>
 static cudaError_t launch_prefill_t(const PrefillParams& p, const PrefillTensors& T, cudaStream_t stream) {
   CUtensorMap mq, mkc, mvc, mkp, mvp;
@@ -554,7 +620,8 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const PrefillTensors
   const int smem = PfLayout<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(msa_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int grid = p.n_work < num_sms() ? p.n_work : num_sms();
+
+  const int grid = p.n_ctas;  // the planner balanced the pieces over this many CTAs
   if (grid == 0) return cudaSuccess;
   msa_prefill_kernel<D><<<grid, kPfThreads, smem, stream>>>(mq, mkc, mvc, mkp, mvp, p);
   return cudaGetLastError();

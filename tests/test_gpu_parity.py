@@ -25,17 +25,17 @@ def built():
     msa.lib()
 
 
-def run_prefill(lay, wl=None, **kw):
+def run_prefill(lay, wl=None, plan_kw=None, **kw):
     wl = wl or W.make_values(lay, device="cuda")
-    plan = msa.Plan.from_layout(lay).upload("cuda")
+    plan = msa.Plan.from_layout(lay, **(plan_kw or {})).upload("cuda")
     out, lse = msa.prefill(plan, wl.q, wl.k_chunk, wl.v_chunk, wl.k_pool, wl.v_pool, **kw)
     torch.cuda.synchronize()
     assert msa.get_status(plan) == 0
     return wl, out, lse
 
 
-def check_prefill(lay, rows=None, scale=None, wl=None):
-    wl, out, lse = run_prefill(lay, wl, scale=scale)
+def check_prefill(lay, rows=None, scale=None, wl=None, plan_kw=None):
+    wl, out, lse = run_prefill(lay, wl, plan_kw, scale=scale)
     a = workload_arrays(wl)
     sc = 1.0 / math.sqrt(lay.head_dim) if scale is None else scale
     rows_, ref_o, ref_l = O.prefill(lay, a["q"], a["k_chunk"], a["v_chunk"], a["k_pool"], a["v_pool"], sc,
@@ -316,3 +316,33 @@ def test_prefill_deterministic_and_permutation_invariant():
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 5, 37, 148, 1000])
+def test_prefill_schedules(ctas):
+    """The same layout balanced over different CTA counts: whole items, items cut into
+    2 or more pieces merged on the device; every schedule matches the oracle and is
+    bit-reproducible."""
+    rng = np.random.default_rng(31)
+    specs = [W.random_prefill_spec(rng, 90, 0.5, 120, 900), W.random_prefill_spec(rng, 30, 0.3, 40, 300)]
+    lay = W.custom_prefill(8, 2, 128, specs, seed=31, qk_std=0.5)
+    plan = msa.Plan.from_layout(lay, prefill_ctas=ctas)
+    sc = plan.export_schedule()
+    if ctas >= 37:
+        assert (sc[:, 6] > 1).any()          # some items are split and merged
+    wl, o1, l1 = check_prefill(lay, plan_kw={"prefill_ctas": ctas})
+    _, o2, l2 = run_prefill(lay, wl, {"prefill_ctas": ctas})
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_prefill_split_sharp_logits():
+    """Items cut into pieces whose maxima differ by a lot (unscaled logits, planted keys):
+    the log-sum-exp merge of the pieces must still match the oracle."""
+    rng = np.random.default_rng(32)
+    spec = W.random_prefill_spec(rng, 120, 0.6, 64, 1024)
+    lay = W.custom_prefill(4, 1, 128, [spec], seed=32, qk_std=1.0)
+    wl = W.make_values(lay, device="cuda")
+    for _ in range(12):
+        b = int(rng.integers(0, lay.num_pool_blocks))
+        wl.k_pool[b, :, int(rng.integers(0, 16)), :] = wl.q[int(rng.integers(0, lay.total_q)), :1, :] * 4
+    check_prefill(lay, wl=wl, plan_kw={"prefill_ctas": 64})

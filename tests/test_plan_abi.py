@@ -198,3 +198,64 @@ def test_decode_needs_one_query_per_sequence():
         msa.Plan("decode", 4, 2, 64, lay.segments, lay.block_table, lay.block_pos, lay.block_fill,
                  np.array([0, 2], np.int32))
     assert e.value.code == -1
+
+
+def _list_counts(plan):
+    """Non-skipped KV tiles of every query tile, from the canonical export."""
+    c = plan.export()
+    _, _, ntok, nkt, nqt, ncls = c[:6]
+    off = 6 + 4 * ntok
+    kts = c[off:off + 6 * nkt].reshape(-1, 6)
+    off += 6 * nkt
+    qts = c[off:off + 5 * nqt].reshape(-1, 5)
+    off += 5 * nqt
+    cls = c[off:off + ncls]
+    out, ci = [], 0
+    for q in qts:
+        n = int((kts[:, 0] == q[0]).sum())
+        out.append(int((cls[ci:ci + n] != 0).sum()))
+        ci += n
+    return out
+
+
+@pytest.mark.parametrize("idx,ctas", [(1, 0), (2, 0), (2, 1), (2, 7), (2, 500), (3, 0), (5, 0)])
+def test_prefill_schedule_covers_every_item_once(idx, ctas):
+    lay = W.make_layout(idx, tiler=msa.chunk_sizes)
+    plan = msa.Plan.from_layout(lay, prefill_ctas=ctas)
+    sc = plan.export_schedule()
+    st = plan.stats()
+    counts = _list_counts(plan)
+    G = lay.num_heads_q // lay.num_heads_kv
+    hpc = 2 if G % 2 == 0 else 1
+    n_ctas = st["num_prefill_ctas"]
+    assert 1 <= n_ctas <= (ctas or 148)
+    assert np.all(np.diff(sc[:, 0]) >= 0) and set(sc[:, 0]) == set(range(n_ctas))
+    assert st["num_work_items"] == len(sc)
+    pieces = {}
+    for (c, qt, g, h0, j0, n, nparts, slot0, slot) in sc:
+        assert n >= 1 and 0 <= g < lay.num_heads_kv and h0 % hpc == 0 and h0 // G == g
+        pieces.setdefault((qt, g, h0), []).append((j0, n, nparts, slot0, slot))
+    # every (query tile, KV head, head pair) exactly once, its list covered in slot order
+    assert len(pieces) == len(counts) * lay.num_heads_kv * (G // hpc)
+    slots = []
+    for (qt, g, h0), ps in pieces.items():
+        ps.sort()
+        assert all(p[2] == len(ps) for p in ps)
+        assert ps[0][0] == 0 and sum(p[1] for p in ps) == counts[qt]
+        assert all(a[0] + a[1] == b[0] for a, b in zip(ps[:-1], ps[1:]))
+        if len(ps) == 1:
+            assert ps[0][3] == -1 and ps[0][4] == -1
+        else:
+            assert [p[4] for p in ps] == [ps[0][3] + k for k in range(len(ps))]
+            slots += [p[4] for p in ps]
+    assert len(set(slots)) == len(slots)
+    assert st["num_split_items"] == sum(1 for ps in pieces.values() if len(ps) > 1)
+
+
+def test_prefill_schedule_balance():
+    """The Llama-3-8B-shaped layer (16 query tiles x 16 head pairs, 32-74 KV tiles each)
+    balances to within a few percent over 148 CTAs once items may be cut."""
+    lay = W.make_layout(2)
+    sc = msa.Plan.from_layout(lay).export_schedule()
+    load = np.bincount(sc[:, 0], weights=sc[:, 5])
+    assert load.max() <= 1.04 * load.mean()
