@@ -8,28 +8,31 @@
 // causally by original position.  One launch covers all sequences; outputs O (bf16)
 // and the natural-log LSE (fp32).
 //
-// How (one persistent CTA per SM, warp-specialised, 320 threads):
-//  * warp 9 (producer): TMA loads of the Q tiles (two query heads sharing one KV head,
-//    128 chunk rows each), of each K tile into a 3-deep ring and of each V tile into a
-//    2-deep ring (a K slot frees as soon as its QK^T is done, so K runs well ahead).  A pool KV tile is 8
+// How (one persistent CTA per SM, warp-specialised, 12 warps in 3 warpgroups):
+//  * warp 10 (K producer): TMA loads of the Q tiles (two query heads sharing one KV head,
+//    128 chunk rows each) and of each K tile into a 3-deep ring.  A pool KV tile is 8
 //    paged blocks, one 16-row box per block and 64-column slab; a chunk KV tile is one
 //    128-row box per slab.  Missing blocks of a short pool tile are loaded from an
-//    out-of-range row and arrive as zeros.  The producer also writes each tile's 128
-//    key positions to shared memory for the masking of partial tiles.
+//    out-of-range row and arrive as zeros.
+//  * warp 11 (V producer): the V tiles into a 2-deep ring, and for each tile a mask
+//    record (per 16-row block: the position or chunk row of its first key and its
+//    number of valid keys) used by partial tiles.
 //  * warp 8 (MMA issuer, one thread): tcgen05.mma kind::f16.  S_t = Q_t K^T (both
 //    operands in 128-byte-swizzled shared memory, accumulator in TMEM), then
 //    O_t += P_t V with P_t read from TMEM (it overwrites S_t as bf16) and V as an
 //    MN-major shared-memory operand.  The two heads ping-pong: while one softmax group
 //    works on S_0, the tensor core runs the other head's GEMMs.
 //  * warps 0-3 / 4-7 (softmax groups, one per head): each thread owns one query row in
-//    TMEM (tcgen05.ld 32x32b), applies the position mask on partial tiles only, keeps the
-//    running max in log2 units, rescales the O accumulator in TMEM only when the max
-//    grows by more than 2^8 (the result is exact either way: the final O is divided by
-//    the sum taken with the same reference max), writes P as bf16 back to TMEM, and
-//    at the end normalises O and stores bf16 rows and the LSE.
+//    TMEM (tcgen05.ld 32x32b), masks partial tiles by a per-block prefix cut, takes the
+//    exponentials against the running reference max while finding the tile max in the
+//    same pass (re-doing the pass only if the max grew by more than 2^8), writes P as
+//    bf16 back to TMEM, and at the end normalises O and stores bf16 rows and the LSE.
 //  * KV tiles whose smallest position exceeds the query tile's largest are never
 //    loaded (the planner leaves them out of the work item's list); tiles that every
 //    query row sees fully skip the mask.
+//  * Registers: the softmax warpgroups hold a full 128-column row of S and run with 216
+//    registers a thread; the third warpgroup (MMA issuer, producers) gives its share
+//    back (setmaxnreg).
 // TMEM: 512 columns = S_0 | S_1 | O_0 | O_1 (128 columns each).
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -39,22 +42,30 @@
 
 namespace msa {
 
-
-constexpr int kPfThreads = 320;
+// 12 warps = 3 full warpgroups (setmaxnreg acts on whole warpgroups); warp 9 idles.
+// At launch every thread gets kPfLaunchRegs registers (65536 / 384, rounded down to 8);
+// the split below must fit in that total, and the host refuses to launch a build whose
+// kernel was given fewer registers.
+constexpr int kPfThreads = 384;
+constexpr int kPfLaunchRegs = 168;
+constexpr int kPfRegsSoftmax = 216;    // after setmaxnreg, warpgroups 0-1
+constexpr int kPfRegsOther = 64;       // after setmaxnreg, warpgroup 2
+static_assert(2 * 128 * kPfRegsSoftmax + 128 * kPfRegsOther <= kPfThreads * kPfLaunchRegs, "register split");
 constexpr int kKStages = 3;            // K tiles in flight (a slot frees once its QK^T is done)
 constexpr int kVStages = 2;            // V tiles (a slot frees once its PV is done)
 constexpr int kSlabBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
+constexpr int kMaskInts = 20;          // mask record: base[8], nvalid[8], src, pad[3]
 
-// Shared memory: small items first (barriers, key positions), then the operand tiles on
+// Shared memory: small items first (barriers, mask records), then the operand tiles on
 // a 1024-byte boundary (the 128-byte swizzle pattern repeats every 1024 bytes).
 template <int D>
 struct PfLayout {
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kNumBars = 27;
+  static constexpr int kNumBars = 28;
   static constexpr int kBar = 0;
-  static constexpr int kMisc = (kBar + kNumBars * 8 + 15) / 16 * 16;  // TMEM base address, abort flag
-  static constexpr int kPos = (kMisc + 16 + 127) / 128 * 128;          // int32 [kVStages][128], read as int4
-  static constexpr int kSmall = kPos + kVStages * 128 * 4;
+  static constexpr int kMisc = (kBar + kNumBars * 8 + 15) / 16 * 16;  // TMEM base address, flags
+  static constexpr int kMask = kMisc + 16;                             // int32 [kVStages][kMaskInts]
+  static constexpr int kSmall = kMask + kVStages * kMaskInts * 4;
   static constexpr int kQ = 0;                         // offsets from the aligned tile base
   static constexpr int kK = kQ + 2 * kTileBytes;
   static constexpr int kV = kK + kKStages * kTileBytes;
@@ -62,7 +73,7 @@ struct PfLayout {
   static constexpr int kBytes = kSmall + 1023 + kTiles;
 };
 static_assert(PfLayout<128>::kBytes <= 232448, "prefill shared memory exceeds 227 KB");
-static_assert(PfLayout<128>::kPos % 16 == 0 && PfLayout<128>::kMisc % 16 == 0, "16-byte alignment");
+static_assert(PfLayout<128>::kMask % 16 == 0 && PfLayout<128>::kMisc % 16 == 0, "16-byte alignment");
 
 // Bounded wait that also gives up as soon as another role of this CTA gave up.
 __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, const PrefillParams& p,
@@ -160,18 +171,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* k_empty = bars + 5;    // [3]
   uint64_t* v_full = bars + 8;     // [2]
   uint64_t* v_empty = bars + 10;   // [2]
-  uint64_t* pos_full = bars + 12;  // [2] key positions of the tile held in V slot s
+  uint64_t* m_full = bars + 12;    // [2] mask record of the tile held in V slot s
   uint64_t* s_full = bars + 14;    // [2] per head
   uint64_t* p_full = bars + 16;    // [2]
   uint64_t* o_full = bars + 18;    // [2]
   uint64_t* o_free = bars + 20;    // [2]
-  uint64_t* drain = bars + 22;
-  uint64_t* ep_bar = bars + 23;    // [2] split pieces: the head's 128 threads stored their partial
-  uint64_t* ep_flag = bars + 25;   // [2] split pieces: merge counter read, last_flag[t] valid
+  uint64_t* drain = bars + 22;    // [2] one per MMA-issuing thread
+  uint64_t* ep_bar = bars + 24;    // [2] split pieces: the head's 128 threads stored their partial
+  uint64_t* ep_flag = bars + 26;   // [2] split pieces: merge counter read, last_flag[t] valid
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + L::kMisc + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem_raw + L::kMisc + 8);  // [2]
-  int32_t* sPos = reinterpret_cast<int32_t*>(smem_raw + L::kPos);
+  int32_t* sMask = reinterpret_cast<int32_t*>(smem_raw + L::kMask);
   uint8_t* tiles = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw + L::kSmall) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = tiles + L::kQ;
@@ -179,6 +190,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint8_t* sV = tiles + L::kV;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta_w0 = __ldg(p.cta_begin + blockIdx.x), cta_w1 = __ldg(p.cta_begin + blockIdx.x + 1);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -190,19 +202,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
-      mbar_init(&pos_full[s], 1);
+      mbar_init(&m_full[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 128);
       mbar_init(&o_full[t], 1);
       mbar_init(&o_free[t], 128);
-    }
-    mbar_init(drain, 1);
-    for (int t = 0; t < 2; ++t) {
       mbar_init(&ep_bar[t], 128);
       mbar_init(&ep_flag[t], 1);
     }
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -215,23 +226,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 9) {
-    // ------------------------------------------------------------ producer
-    // Per work item: Q, K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1).  K(j) waits for
-    // the QK^T of the tile three back in its slot; V(j) waits for the PV of the tile two
-    // back, which also frees that slot's key positions (that tile's softmax is done).
-    int kit = 0, vit = 0, wi = 0;  // K tiles, V tiles and work items issued
+  // The two register regions never merge again: each ends with its own barrier and
+  // return, so the compiler can give each the register budget of its warpgroups.
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
+  if (warp == 10) {
+    // ------------------------------------------------------------ K producer (and Q)
+    int kit = 0, wi = 0;  // K tiles and work items issued
     int last_k[kKStages] = {-1, -1, -1};
-    int last_v[kVStages] = {-1, -1};
     int last_wi = -1;
-    for (int w = __ldg(p.cta_begin + blockIdx.x), w1 = __ldg(p.cta_begin + blockIdx.x + 1); w < w1; ++w) {
+    for (int w = cta_w0; w < cta_w1; ++w) {
       const WorkRec wk = p.work[w];
       const QTileRec qt = p.qt[wk.qt];
       const int n = wk.n;
       if (n == 0) continue;
       const int* lst = p.list + qt.list_begin + wk.j0;
       TileRec cur = load_tile_rec(p, lst, 0, lane);
-      if (!pf_wait_warp(q_empty, (wi & 1) ^ 1, p, abort_flag)) goto producer_done;
+      if (!pf_wait_warp(q_empty, (wi & 1) ^ 1, p, abort_flag)) goto kprod_done;
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, p.hpc * L::kTileBytes);
         for (int t = 0; t < p.hpc; ++t)
@@ -239,128 +250,149 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tma_load_2d(sQ + t * L::kTileBytes + s * kSlabBytes, &tm_q, q_full, (wk.h0 + t) * D + s * 64, qt.row0);
       }
       last_wi = wi;
-      TileRec prev = cur;
-      for (int j = 0; j <= n; ++j) {
+      for (int j = 0; j < n; ++j) {
         TileRec nxt = cur;
         if (j + 1 < n) nxt = load_tile_rec(p, lst, j + 1, lane);
-        if (j < n) {
-          const int ks = kit % kKStages;
-          if (!pf_wait_warp(&k_empty[ks], ((kit / kKStages) & 1) ^ 1, p, abort_flag)) goto producer_done;
-          issue_kv_tile<D>(cur, sK + ks * L::kTileBytes, &k_full[ks], &tm_kc, &tm_kp, wk.g, p.Hkv, p.pool_rows,
-                           lane);
-          last_k[ks] = kit;
-          ++kit;
-        }
-        if (j >= 1) {
-          // V and key positions of the previous tile
-          const int vs = vit % kVStages;
-          if (!pf_wait_warp(&v_empty[vs], ((vit / kVStages) & 1) ^ 1, p, abort_flag)) goto producer_done;
-          issue_kv_tile<D>(prev, sV + vs * L::kTileBytes, &v_full[vs], &tm_vc, &tm_vp, wk.g, p.Hkv, p.pool_rows,
-                           lane);
-          last_v[vs] = vit;
-          const int src = prev.get(0), ntok = prev.get(1), row0 = prev.get(2), nblk = prev.get(3);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int r = q4 * 32 + lane;
-            const int i = r >> 4, tt = r & 15;
-            const int bp = prev.get(16 + i);
-            const int bf = prev.get(24 + i);
-            int pos;
-            if (src == SRC_CHUNK) pos = (r < ntok) ? __ldg(p.qpos + row0 + r) : 0x7fffffff;
-            else pos = (i < nblk && tt < bf) ? bp + tt : 0x7fffffff;
-            sPos[vs * 128 + r] = pos;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&pos_full[vs]);
-          ++vit;
-        }
-        prev = cur;
+        const int ks = kit % kKStages;
+        if (!pf_wait_warp(&k_empty[ks], ((kit / kKStages) & 1) ^ 1, p, abort_flag)) goto kprod_done;
+        issue_kv_tile<D>(cur, sK + ks * L::kTileBytes, &k_full[ks], &tm_kc, &tm_kp, wk.g, p.Hkv, p.pool_rows, lane);
+        last_k[ks] = kit;
+        ++kit;
         cur = nxt;
       }
       ++wi;
     }
-  producer_done:
+  kprod_done:
     // every copy this warp started must land before the CTA may exit
     for (int s = 0; s < kKStages; ++s)
       if (last_k[s] >= 0) mbar_wait(&k_full[s], (last_k[s] / kKStages) & 1, 1000000000ull);
+    if (last_wi >= 0) mbar_wait(q_full, last_wi & 1, 1000000000ull);
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ V producer (and mask records)
+    int vit = 0;
+    int last_v[kVStages] = {-1, -1};
+    for (int w = cta_w0; w < cta_w1; ++w) {
+      const WorkRec wk = p.work[w];
+      const QTileRec qt = p.qt[wk.qt];
+      const int n = wk.n;
+      if (n == 0) continue;
+      const int* lst = p.list + qt.list_begin + wk.j0;
+      TileRec cur = load_tile_rec(p, lst, 0, lane);
+      for (int j = 0; j < n; ++j) {
+        TileRec nxt = cur;
+        if (j + 1 < n) nxt = load_tile_rec(p, lst, j + 1, lane);
+        const int vs = vit % kVStages;
+        if (!pf_wait_warp(&v_empty[vs], ((vit / kVStages) & 1) ^ 1, p, abort_flag)) goto vprod_done;
+        issue_kv_tile<D>(cur, sV + vs * L::kTileBytes, &v_full[vs], &tm_vc, &tm_vp, wk.g, p.Hkv, p.pool_rows, lane);
+        last_v[vs] = vit;
+        // mask record: per 16-row block i, the first key's position (pool) or chunk row
+        // (chunk) and the number of valid keys; chunk tiles are compared by row index
+        // (chunk rows of one sequence are in position order)
+        {
+          const int src = cur.get(0), ntok = cur.get(1), row0 = cur.get(2), nblk = cur.get(3);
+          const int i = lane & 7;
+          const int bp = cur.get(16 + i), bf = cur.get(24 + i);
+          int val = 0;
+          if (lane < 8) {
+            val = (src == SRC_CHUNK) ? row0 + 16 * i : bp;
+          } else if (lane < 16) {
+            val = (src == SRC_CHUNK) ? min(max(ntok - 16 * i, 0), 16) : (i < nblk ? bf : 0);
+          } else if (lane == 16) {
+            val = src;
+          }
+          if (lane < kMaskInts) sMask[vs * kMaskInts + lane] = val;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&m_full[vs]);
+        }
+        ++vit;
+        cur = nxt;
+      }
+    }
+  vprod_done:
     for (int s = 0; s < kVStages; ++s)
       if (last_v[s] >= 0) mbar_wait(&v_full[s], (last_v[s] / kVStages) & 1, 1000000000ull);
-    if (last_wi >= 0) mbar_wait(q_full, last_wi & 1, 1000000000ull);
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int it = 0, wi = 0;
-      auto issue_qk = [&](int t, int ks) {
-        const uint32_t qa = smem_u32(sQ + t * L::kTileBytes);
-        const uint32_t ka = smem_u32(sK + ks * L::kTileBytes);
+      // descriptors of every operand buffer, built once; the k-step offsets add to the
+      // start-address field (addresses stay below 2^18, so the field never overflows)
+      uint64_t qd[2], kd[kKStages], vd[kVStages];
+      for (int t = 0; t < 2; ++t) qd[t] = smem_desc_sw128(smem_u32(sQ + t * L::kTileBytes), 16, 1024);
+      for (int s = 0; s < kKStages; ++s) kd[s] = smem_desc_sw128(smem_u32(sK + s * L::kTileBytes), 16, 1024);
+      for (int s = 0; s < kVStages; ++s) vd[s] = smem_desc_sw128(smem_u32(sV + s * L::kTileBytes), kSlabBytes, 1024);
+      int it = 0, wi = 0, ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;  // phase bits of the K and V rings at (ks, vs)
+      auto issue_qk = [&](int t, int kslot) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
-          umma_ss(tmem + t * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                  kIdescQK, kk > 0);
+          const uint64_t off = (uint64_t)((((kk >> 2) * kSlabBytes) + (kk & 3) * 32) >> 4);
+          umma_ss(tmem + t * 128, qd[t] + off, kd[kslot] + off, kIdescQK, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, int vs, bool acc) {
-        const uint32_t va = smem_u32(sV + vs * L::kTileBytes);
+      auto issue_pv = [&](int t, int vslot, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                  smem_desc_sw128(va + kk * 2048, kSlabBytes, 1024), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vd[vslot] + (uint64_t)((kk * 2048) >> 4),
+                  kIdescPV, (acc || kk > 0) ? 1u : 0u);
       };
-      for (int w = __ldg(p.cta_begin + blockIdx.x), w1 = __ldg(p.cta_begin + blockIdx.x + 1); w < w1; ++w) {
+      for (int w = cta_w0; w < cta_w1; ++w) {
         const int n = p.work[w].n;
         if (n == 0) continue;
         if (!pf_wait(q_full, wi & 1, p, abort_flag)) goto mma_done;
-        {
-          const int ks0 = it % kKStages;
-          if (!pf_wait(&k_full[ks0], (it / kKStages) & 1, p, abort_flag)) goto mma_done;
-          tc_fence_after();
-          for (int t = 0; t < p.hpc; ++t) {
-            issue_qk(t, ks0);
-            umma_commit(&s_full[t]);
-          }
-          umma_commit(&k_empty[ks0]);
-          if (n == 1) umma_commit(q_empty);
+        if (!pf_wait(&k_full[ks], kph, p, abort_flag)) goto mma_done;
+        tc_fence_after();
+        for (int t = 0; t < p.hpc; ++t) {
+          issue_qk(t, ks);
+          umma_commit(&s_full[t]);
         }
+        if (n == 1) umma_commit(q_empty);
+        if (++ks == kKStages) { ks = 0; kph ^= 1; }
         for (int j = 0; j < n; ++j) {
-          const int cur = it + j, vs = cur % kVStages;
-          const int nxt = cur + 1, ksn = nxt % kKStages;
+          const int cur = it + j;
           const bool has_next = j + 1 < n;
-          bool have_v = false, have_kn = false;
           for (int t = 0; t < p.hpc; ++t) {
             if (!pf_wait(&p_full[t], cur & 1, p, abort_flag)) goto mma_done;
-            if (j == 0 && !pf_wait(&o_free[t], (wi & 1) ^ 1, p, abort_flag)) goto mma_done;
-            if (!have_v) {
-              if (!pf_wait(&v_full[vs], (cur / kVStages) & 1, p, abort_flag)) goto mma_done;
-              have_v = true;
+            if (t == 0) {
+              if (j == 0 && !pf_wait(&o_free[0], (wi & 1) ^ 1, p, abort_flag)) goto mma_done;
+              if (!pf_wait(&v_full[vs], vph, p, abort_flag)) goto mma_done;
+              if (has_next && !pf_wait(&k_full[ks], kph, p, abort_flag)) goto mma_done;
+            } else if (j == 0 && !pf_wait(&o_free[t], (wi & 1) ^ 1, p, abort_flag)) {
+              goto mma_done;
             }
             tc_fence_after();
             issue_pv(t, vs, j > 0);
             if (has_next) {
-              if (!have_kn) {
-                if (!pf_wait(&k_full[ksn], (nxt / kKStages) & 1, p, abort_flag)) goto mma_done;
-                have_kn = true;
-                tc_fence_after();
-              }
-              issue_qk(t, ksn);
+              issue_qk(t, ks);
               umma_commit(&s_full[t]);
             } else {
               umma_commit(&o_full[t]);
             }
           }
-          if (has_next) umma_commit(&k_empty[ksn]);
+          // the K and V slots are handed back by the last softmax group once it sees
+          // the S (or O) that these GEMMs produced: that commit covers every MMA above
+          if (has_next && ++ks == kKStages) { ks = 0; kph ^= 1; }
           if (j + 2 == n) umma_commit(q_empty);
-          umma_commit(&v_empty[vs]);
+          if (++vs == kVStages) { vs = 0; vph ^= 1; }
         }
         it += n;
         ++wi;
       }
     mma_done:
-      umma_commit(drain);
-      mbar_wait(drain, 0, 1000000000ull);
+      umma_commit(&drain[0]);
+      mbar_wait(&drain[0], 0, 1000000000ull);
     }
     __syncwarp();
-  } else {
+  }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+    return;
+  }
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPfRegsSoftmax));
+  {
     // ------------------------------------------------------------ softmax groups
     const int t = warp >> 2, wq = warp & 3;
     const int r = wq * 32 + lane;
@@ -369,7 +401,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tO = tmem + lane_base + 256 + t * 128;
     const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
     int it = 0, wi = 0, se = 0;  // tiles, pieces and split pieces done
-    for (int w = __ldg(p.cta_begin + blockIdx.x), w1 = __ldg(p.cta_begin + blockIdx.x + 1); w < w1; ++w) {
+    for (int w = cta_w0; w < cta_w1; ++w) {
       const WorkRec wk = p.work[w];
       const QTileRec qt = p.qt[wk.qt];
       const int n = wk.n;
@@ -381,7 +413,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       const int h = wk.h0 + t;
       const bool valid = r < qt.nrows;
-      const int qp = valid ? __ldg(p.qpos + qt.row0 + r) : -1;
+      const bool releaser = t == p.hpc - 1;
+      // rows past the tile's end see every key (their values are finite and never stored)
+      const int qp = valid ? __ldg(p.qpos + qt.row0 + r) : 0x7fffffff;
+      const int qrow = valid ? qt.row0 + r : 0x7fffffff;
       float m_used = -INFINITY, l = 0.f;
       const int* lst = p.list + qt.list_begin + wk.j0;
       int e_next = __ldg(lst);
@@ -390,41 +425,97 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const bool partial = e_next < 0;
         if (j + 1 < n) e_next = __ldg(lst + j + 1);
         if (!pf_wait_warp(&s_full[t], it & 1, p, abort_flag)) goto softmax_done;
+        if (releaser && lane == 0 && wq == 0) {
+          // S of this tile for the last head is done: every MMA issued before it is too,
+          // so this tile's K slot and the previous tile's V slot are free
+          mbar_arrive(&k_empty[it % kKStages]);
+          if (j > 0) mbar_arrive(&v_empty[(it - 1) % kVStages]);
+        }
         tc_fence_after();
         uint32_t s[128];
-        tmem_ld_x32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        tmem_ld_x32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-        tmem_ld_x32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+        tmem_ld_x64(tS + 0, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
+        tmem_ld_x64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&s[64]));
         tmem_wait_ld();
         if (partial) {
-          if (!pf_wait_warp(&pos_full[vs], (it / kVStages) & 1, p, abort_flag)) goto softmax_done;
-          const int4* kp4 = reinterpret_cast<const int4*>(sPos + vs * 128);
+          // key (block b, slot u) is visible iff u < cut_b, cut_b = clamp(ref - base_b + 1, 0, nvalid_b)
+          if (!pf_wait_warp(&m_full[vs], (it / kVStages) & 1, p, abort_flag)) goto softmax_done;
+          const int4* mr = reinterpret_cast<const int4*>(sMask + vs * kMaskInts);
+          const int4 b0 = mr[0], b1 = mr[1], f0 = mr[2], f1 = mr[3], sx = mr[4];
+          const int ref = sx.x == SRC_CHUNK ? qrow : qp;
+          const int base[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+          const int nv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int4 kp = kp4[c];
-            if (kp.x > qp) s[4 * c + 0] = __float_as_uint(-INFINITY);
-            if (kp.y > qp) s[4 * c + 1] = __float_as_uint(-INFINITY);
-            if (kp.z > qp) s[4 * c + 2] = __float_as_uint(-INFINITY);
-            if (kp.w > qp) s[4 * c + 3] = __float_as_uint(-INFINITY);
+          for (int b = 0; b < 8; ++b) {
+            // ref - base + 1 cannot overflow: a row past the end uses INT_MAX only against
+            // bases >= 0, and then the cut is the block's valid count
+            const int d = ref - base[b];
+            const int cut = d < 0 ? 0 : (d >= nv[b] ? nv[b] : d + 1);
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+              if (u >= cut) s[16 * b + u] = __float_as_uint(-INFINITY);
           }
         }
-        // row max: eight independent chains, then a tree
-        float m8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(s[i]);
-#pragma unroll
-        for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(s[c]));
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        const float m_cand = mx * p.scale_log2;
-        const bool need = m_cand > m_used + 8.f;
-        const bool resc = need && (m_used != -INFINITY);
+        // Exponents are taken against the reference max m_used of the earlier tiles
+        // while this tile's max is found in the same pass (the two chains interleave).
+        // Only if the tile's max exceeds the reference by more than 2^8 is the pass
+        // redone against the new max, with O and l rescaled.  The first tile of a piece
+        // (reference still -inf) finds its max first.
         float factor = 1.f;
-        if (need) {
-          if (resc) factor = fast_exp2(m_used - m_cand);
-          l *= factor;
-          m_used = m_cand;
+        bool resc = false;
+        const bool spec = !__any_sync(0xffffffffu, m_used == -INFINITY);
+        if (!spec) {
+          float m4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) m4[i] = fmax3(__uint_as_float(s[i]), __uint_as_float(s[4 + i]), -INFINITY);
+#pragma unroll
+          for (int c = 8; c < 128; c += 8)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              m4[i] = fmax3(m4[i], __uint_as_float(s[c + i]), __uint_as_float(s[c + 4 + i]));
+          const float m_cand = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * p.scale_log2;
+          if (m_cand > m_used + 8.f) {
+            resc = m_used != -INFINITY;
+            if (resc) factor = fast_exp2(m_used - m_cand);
+            l *= factor;
+            m_used = m_cand;
+          }
+        }
+        float2 acc[4];
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+          const float ms = (m_used == -INFINITY) ? 0.f : m_used;
+          const float2 nms2 = make_float2(-ms, -ms);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int e = q * 32 + 2 * c;
+              const float2 x = ffma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), scale2, nms2);
+              const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+              acc[c & 3] = fadd2(acc[c & 3], pe);
+              pk[c] = pack_bf16x2(pe.x, pe.y);
+              if (c & 1)
+                m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], fmax3(__uint_as_float(s[e - 2]), __uint_as_float(s[e - 1]),
+                                                                 __uint_as_float(s[e])),
+                                         __uint_as_float(s[e + 1]));
+            }
+            tmem_st_x16(tS + q * 16, pk);
+          }
+          if (pass == 1 || !spec) break;
+          const float m_cand = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * p.scale_log2;
+          const bool redo = m_cand > m_used + 8.f;
+          if (!__any_sync(0xffffffffu, redo)) break;
+          if (redo) {
+            factor = fast_exp2(m_used - m_cand);
+            l *= factor;
+            m_used = m_cand;
+            resc = true;
+          }
+          tmem_wait_st();  // the second pass overwrites these P columns
         }
         if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
@@ -436,31 +527,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * factor);
             tmem_st_x32(tO + c, ov);
           }
-          tmem_wait_st();
-        }
-        const float ms = (m_used == -INFINITY) ? 0.f : m_used;
-        const float2 nms2 = make_float2(-ms, -ms);
-        float2 acc[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float2 x =
-              ffma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), scale2, nms2);
-          const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          acc[c & 3] = fadd2(acc[c & 3], pe);
-          s[c] = pack_bf16x2(pe.x, pe.y);
         }
         const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
         l += a.x + a.y;
-        tmem_st_x32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
       }
       // epilogue: O / l -> bf16, LSE = ln 2 * (m + log2 l)
       if (!pf_wait_warp(&o_full[t], wi & 1, p, abort_flag)) goto softmax_done;
+      if (releaser && lane == 0 && wq == 0) mbar_arrive(&v_empty[(it - 1) % kVStages]);  // last tile's V
       tc_fence_after();
       if (wk.nparts == 1) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -560,13 +636,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   softmax_done:;
   }
-
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -620,6 +691,11 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const PrefillTensors
   const int smem = PfLayout<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(msa_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // the warpgroups' register split (setmaxnreg) must fit in what the launch allocates
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, msa_prefill_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kPfLaunchRegs) return cudaErrorInvalidConfiguration;
 
   const int grid = p.n_ctas;  // the planner balanced the pieces over this many CTAs
   if (grid == 0) return cudaSuccess;
