@@ -183,7 +183,7 @@ def run_ours(args, world, rank, local):
     do_pf = args.only in (None, "prefill")
     do_dc = args.only in (None, "decode")
     if do_dc:
-        dl = W.make_layout(args.decode_workload)
+        dl = W.make_layout(args.decode_workload, decode_batch=args.decode_batch)
         dw = W.make_values(dl, device=dev)
         dplan = msa.Plan.from_layout(dl).upload(dev)
         dst = dplan.stats()
@@ -447,6 +447,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=2, help="prefill workload (1, 2, 3 or 5)")
     ap.add_argument("--decode-workload", type=int, default=4)
+    ap.add_argument("--decode-batch", type=int, default=64,
+                    help="sequences of the decode workload (64 = the bench line; fewer for profiling captures)")
     ap.add_argument("--cpu-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -386,8 +386,10 @@ def _wl5(rng, seed):
 
 
 def make_layout(index: int, seed: Optional[int] = None,
-                tiler: Optional[Callable[[int, int, int], Sequence[int]]] = None) -> Layout:
-    """Layout of numbered workload ``index`` (1..5)."""
+                tiler: Optional[Callable[[int, int, int], Sequence[int]]] = None,
+                decode_batch: int = 64) -> Layout:
+    """Layout of numbered workload ``index`` (1..5).  ``decode_batch`` shrinks the decode
+    workload (4) to fewer sequences of the same distribution (for small profiling cases)."""
     seed = default_seed(index) if seed is None else int(seed)
     rng = np.random.default_rng(seed)
     if index == 1:
@@ -397,7 +399,10 @@ def make_layout(index: int, seed: Optional[int] = None,
     if index == 3:
         return _wl3(rng, seed, tiler)
     if index == 4:
-        return _wl4(rng, seed)
+        lay = _wl4(rng, seed, batch=decode_batch)
+        if decode_batch != 64:
+            lay.name = f"decode_batch{decode_batch}_ctx4k_64k"
+        return lay
     if index == 5:
         return _wl5(rng, seed)
     raise ValueError(f"unknown workload {index}")
