@@ -118,6 +118,7 @@ extern "C" msa_status_t msa_decode(const msa_plan_t* plan, const void* plan_dev,
   p.Hq = plan->Hq;
   p.Hkv = plan->Hkv;
   p.G = plan->G;
+  p.pool_rows = (int64_t)plan->num_pool_blocks * plan->Hkv * kBlock;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = g_wait_ns.load();
   return launch_decode(p, plan->d, plan->n_split, stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;

@@ -46,6 +46,7 @@ struct DecodeParams {
   int32_t* counters;
   int32_t* status;
   int32_t Hq, Hkv, G;
+  int64_t pool_rows;  // rows of the pool tensors seen as [num_blocks * Hkv * 16][d]
   float scale_log2;
   uint64_t wait_ns;
 };
