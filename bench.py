@@ -283,6 +283,8 @@ def run_ours(args, world, rank, local):
     h2d_dc = hdq.numel() * hdq.element_size()
     d2h_dc = hdout.numel() * hdout.element_size() + hdlse.numel() * hdlse.element_size()
 
+    append = append_bench(msa, W, pl, pw, dev, flush)
+
     result = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -323,6 +325,7 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(flops * world / (e2e_pf * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d_pf + h2d_dc, "d2h_bytes_per_step": d2h_pf + d2h_dc,
                 "prefill_ms": round(e2e_pf, 4), "decode_ms": round(e2e_dc, 4)},
+        "append": append,
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
         "wall_s": round(wall, 3),
@@ -330,6 +333,48 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(pl, pw, args.cpu_rows)
     return result
+
+
+def append_bench(msa, W, pl, pw, dev, flush, reps: int = 20):
+    """Write-back of the prefill chunk's K/V into fresh pool blocks (placement planned on the
+    host, the copy timed on the device; not part of the step).  Bytes = chunk K and V read
+    plus the same written."""
+    import numpy as np
+    import torch
+    n = pl.total_q
+    nblk = n // 16 + 2 * pl.num_seqs + 1
+    kp = torch.zeros(nblk, pl.num_heads_kv, 16, pl.head_dim, dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros_like(kp)
+    bp = np.zeros(nblk, np.int32)
+    bf = np.zeros(nblk, np.int32)
+    dst = []
+    free = list(range(nblk))
+    for s in range(pl.num_seqs):
+        qp = pl.q_pos[pl.cu_q[s]:pl.cu_q[s + 1]]
+        # a chunk that starts part-way into a block continues a block of its own
+        seq_blocks = []
+        if len(qp) and qp[0] % 16:
+            b = free.pop(0)
+            bp[b], bf[b] = qp[0] // 16 * 16, qp[0] % 16
+            seq_blocks = [b]
+        d, new = msa.append_plan(qp, free, bp, bf, seq_blocks=seq_blocks)
+        free = [b for b in free if b not in set(new.tolist())]
+        dst.append(d)
+    slots = torch.from_numpy(np.concatenate(dst).astype(np.int32)).to(dev)
+    for _ in range(3):
+        msa.kv_append(slots, pw.k_chunk, pw.v_chunk, kp, vp)
+    ts = []
+    for _ in range(reps):
+        flush.fill_(3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        msa.kv_append(slots, pw.k_chunk, pw.v_chunk, kp, vp)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = statistics.median(ts)
+    nbytes = 2 * 2 * n * pl.num_heads_kv * pl.head_dim * 2
+    return {"rows": n, "bytes": nbytes, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
 
 
 def _single_kernel_result(args, world, pl, dl, pst, dst, pf_mean, dc_mean, peaks, peak_kind, clocks):

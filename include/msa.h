@@ -220,6 +220,37 @@ msa_status_t msa_gather(const msa_plan_t* plan, const void* plan_dev,
                         void* k_out, void* v_out, int32_t* pos_out, size_t out_tokens,
                         cudaStream_t stream);
 
+/* Write-back of a chunk's fresh K/V into the paged pool (the step after prefill: the
+ * abstract's recomputed evicted blocks, and the new tokens, go back into pool blocks at
+ * their original positions so later chunks and decode find them).  Host-only planning:
+ *   q_pos[n]            original positions of ONE sequence's chunk rows, strictly ascending
+ *   free_blocks[n_free] physical pool blocks the caller hands out, taken in order
+ *   seq_blocks[n_seq_blocks]  the sequence's blocks already in the pool (any order; may be
+ *                       NULL when 0): a position block that a chunk row continues part-way
+ *                       (e.g. a new turn's suffix after a partial last block) is found here
+ *   block_pos, block_fill [num_pool_blocks]  in/out: set for every block written
+ *   dst_slot[n]         out: pool slot of each row, physical_block * 16 + offset
+ *   new_blocks[n_free]  out: the blocks taken from free_blocks, in position order; *n_new
+ * Rows are grouped by position block (pos / 16) and go to one pool block each, at offset
+ * pos % 16.  A group that starts at offset 0 takes the next free block; one that starts at
+ * offset f > 0 continues the sequence's block whose block_pos is the group's position block
+ * and whose fill is f.  Either way the group must extend its block without a hole.  Errors:
+ * INVALID_ARG (unsorted positions, a hole, no block to continue), WORKSPACE (free_blocks too
+ * short), BLOCK_OOB (a block id outside [0, num_pool_blocks)).  On error nothing is written. */
+msa_status_t msa_append_plan(const int32_t* q_pos, int32_t n, const int32_t* free_blocks, int32_t n_free,
+                             const int32_t* seq_blocks, int32_t n_seq_blocks, int32_t* block_pos,
+                             int32_t* block_fill, int32_t num_pool_blocks, int32_t* dst_slot,
+                             int32_t* new_blocks, int32_t* n_new);
+
+/* Copy rows of the chunk's K and V into their pool slots (bit-exact; asynchronous on
+ * `stream`):  k_pool[dst / 16][g][dst % 16][:] = k_chunk[row][g][:] for every KV head g, and
+ * likewise for V.  dst_slot device int32 [n] (a negative slot skips the row; a slot past the
+ * pool is ignored), k_chunk / v_chunk device bf16 [n][Hkv][d], k_pool / v_pool device bf16
+ * [num_pool_blocks][Hkv][16][d]; 16-byte aligned.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+msa_status_t msa_kv_append(const int32_t* dst_slot, const void* k_chunk, const void* v_chunk,
+                           void* k_pool, void* v_pool, int32_t n, int32_t num_heads_kv, int32_t head_dim,
+                           int32_t num_pool_blocks, cudaStream_t stream);
+
 /* Synchronise `stream`, read and clear the workspace status word.  Returns MSA_OK or
  * the device-side error (e.g. MSA_ERR_TIMEOUT). */
 msa_status_t msa_get_status(void* workspace, cudaStream_t stream);

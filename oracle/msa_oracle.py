@@ -316,3 +316,64 @@ def useful_flops(layout) -> int:
         else:
             total += len(kpos)
     return total * layout.num_heads_q * 4 * layout.head_dim
+
+
+# ----------------------------------------------------------------------------- write-back
+
+def append_plan(q_pos, free_blocks, block_pos, block_fill, seq_blocks=()):
+    """Placement of one sequence's chunk rows in paged pool blocks (write-back).
+
+    The abstract: evicted blocks are recomputed on demand, at their original positions;
+    once recomputed (and for the new tokens) their K/V belongs in the cache again.  The
+    pages give no placement rule; this is the library's rule, stated plainly: the row at
+    position p goes to the pool block that holds position block p // 16, at offset p % 16.
+    A position block first met at offset 0 takes the next free block; one first met
+    part-way continues the sequence's block (among ``seq_blocks``) that holds it.  Slots of
+    a block fill from its current fill upward without holes.
+
+    Returns (dst_slot, new_blocks, block_pos, block_fill) with copies of the two arrays
+    updated; raises ValueError where the library returns an error.
+    """
+    q_pos = [int(x) for x in q_pos]
+    block_pos = np.array(block_pos, np.int64)
+    block_fill = np.array(block_fill, np.int64)
+    if any(b <= a for a, b in zip(q_pos[:-1], q_pos[1:])) or any(p < 0 for p in q_pos):
+        raise ValueError("positions must be non-negative and strictly ascending")
+    owner = {}           # position block -> physical block
+    next_free = 0
+    dst = []
+    for p in q_pos:
+        pb = p // BLOCK
+        if pb not in owner:
+            if p % BLOCK != 0:
+                held = [b for b in seq_blocks if block_fill[b] > 0 and block_pos[b] == pb * BLOCK]
+                if not held:
+                    raise ValueError("a row part-way into a block needs the block that holds it")
+                owner[pb] = int(held[-1])
+            else:
+                if next_free >= len(free_blocks):
+                    raise ValueError("not enough free blocks")
+                owner[pb] = int(free_blocks[next_free])
+                next_free += 1
+                block_pos[owner[pb]] = pb * BLOCK
+                block_fill[owner[pb]] = 0
+        b = owner[pb]
+        if p % BLOCK != block_fill[b]:
+            raise ValueError("a hole inside a block")
+        block_fill[b] += 1
+        dst.append(b * BLOCK + p % BLOCK)
+    return (np.array(dst, np.int64), np.array(free_blocks[:next_free], np.int64), block_pos, block_fill)
+
+
+def append(k_chunk, v_chunk, k_pool, v_pool, dst_slot):
+    """Copy every chunk row's K and V (all KV heads) into its pool slot; rows with a
+    negative slot are skipped.  Returns the new pools (the inputs are not modified)."""
+    k_pool = np.array(k_pool, copy=True)
+    v_pool = np.array(v_pool, copy=True)
+    for row, slot in enumerate(np.asarray(dst_slot)):
+        if slot < 0:
+            continue
+        b, t = divmod(int(slot), BLOCK)
+        k_pool[b, :, t, :] = k_chunk[row]
+        v_pool[b, :, t, :] = v_chunk[row]
+    return k_pool, v_pool

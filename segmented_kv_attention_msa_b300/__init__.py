@@ -72,6 +72,8 @@ EXPORTS = {
     "msa_decode_no_alloc": (_I32, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P]),
     "msa_merge_lse": (_I32, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P]),
     "msa_gather": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "msa_append_plan": (_I32, [_P, _I32, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _I32P]),
+    "msa_kv_append": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P]),
     "msa_get_status": (_I32, [_P, _P]),
     "msa_set_wait_limit": (None, [ctypes.c_int64]),
     "msa_status_string": (ctypes.c_char_p, [_I32]),
@@ -292,6 +294,38 @@ def gather(plan: Plan, k_chunk, v_chunk, k_pool, v_pool, stream=None):
                             _dptr(v_pool), _dptr(k), _dptr(v), _dptr(pos), k.shape[0], _stream(stream)),
            "msa_gather")
     return k[:n], v[:n], pos[:n]
+
+
+def append_plan(q_pos, free_blocks, block_pos, block_fill, seq_blocks=()):
+    """Placement of one sequence's chunk rows in the pool (see msa_append_plan in
+    include/msa.h).  block_pos / block_fill (int32 numpy arrays) are updated in place.
+    Returns (dst_slot int32 [n], new_blocks int32 [n_new])."""
+    q = np.ascontiguousarray(np.asarray(q_pos, np.int32))
+    fb = np.ascontiguousarray(np.asarray(free_blocks, np.int32))
+    sb = np.ascontiguousarray(np.asarray(seq_blocks, np.int32))
+    for a in (block_pos, block_fill):
+        if a.dtype != np.int32 or not a.flags.c_contiguous:
+            raise ValueError("block_pos and block_fill must be contiguous int32 arrays (updated in place)")
+    dst = np.zeros(max(1, len(q)), np.int32)
+    new = np.zeros(max(1, len(fb)), np.int32)
+    n_new = ctypes.c_int32(0)
+    _check(lib().msa_append_plan(_ptr(q), len(q), _ptr(fb), len(fb), _ptr(sb) if sb.size else None, len(sb),
+                                 _ptr(block_pos), _ptr(block_fill), len(block_pos), _ptr(dst), _ptr(new),
+                                 ctypes.byref(n_new)),
+           "msa_append_plan")
+    return dst[:len(q)], new[:n_new.value]
+
+
+def kv_append(dst_slot, k_chunk, v_chunk, k_pool, v_pool, stream=None):
+    """Copy chunk rows of K and V into their pool slots (device, bit-exact)."""
+    import torch
+    for t, n in ((k_chunk, "k_chunk"), (v_chunk, "v_chunk"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _bf16(t, n)
+    if dst_slot.dtype != torch.int32 or not dst_slot.is_cuda or not dst_slot.is_contiguous():
+        raise ValueError("dst_slot must be a contiguous int32 CUDA tensor")
+    n, hkv, d = k_chunk.shape
+    _check(lib().msa_kv_append(_dptr(dst_slot), _dptr(k_chunk), _dptr(v_chunk), _dptr(k_pool), _dptr(v_pool),
+                               n, hkv, d, k_pool.shape[0], _stream(stream)), "msa_kv_append")
 
 
 def get_status(plan: Plan, stream=None) -> int:

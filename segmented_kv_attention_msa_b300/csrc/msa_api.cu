@@ -159,3 +159,19 @@ extern "C" msa_status_t msa_gather(const msa_plan_t* plan, const void* plan_dev,
   p.d = plan->d;
   return launch_gather(p, plan->n_gather, stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
+
+extern "C" msa_status_t msa_kv_append(const int32_t* dst_slot, const void* k_chunk, const void* v_chunk,
+                                      void* k_pool, void* v_pool, int32_t n, int32_t num_heads_kv,
+                                      int32_t head_dim, int32_t num_pool_blocks, cudaStream_t stream) {
+  if (n < 0 || num_heads_kv <= 0 || num_pool_blocks < 0) return MSA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MSA_ERR_UNSUPPORTED;
+  if (n == 0) return MSA_OK;
+  if (!dst_slot || !k_chunk || !v_chunk || !k_pool || !v_pool) return MSA_ERR_INVALID_ARG;
+  const void* ptrs[] = {dst_slot, k_chunk, v_chunk, k_pool, v_pool};
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return MSA_ERR_INVALID_ARG;
+  return launch_kv_append(dst_slot, k_chunk, v_chunk, k_pool, v_pool, n, num_heads_kv, head_dim, num_pool_blocks,
+                          stream) == cudaSuccess
+             ? MSA_OK
+             : MSA_ERR_CUDA;
+}

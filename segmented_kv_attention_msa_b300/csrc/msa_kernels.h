@@ -70,5 +70,7 @@ cudaError_t launch_decode(const DecodeParams& p, int d, int n_split, cudaStream_
 cudaError_t launch_merge_lse(const float* oa, const float* la, const float* ob, const float* lb, void* o,
                              float* lse, int64_t n_rh, int d, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, int n_units, cudaStream_t stream);
+cudaError_t launch_kv_append(const int32_t* dst_slot, const void* kc, const void* vc, void* kp, void* vp, int64_t n,
+                             int Hkv, int d, int64_t pool_blocks, cudaStream_t stream);
 
 }  // namespace msa

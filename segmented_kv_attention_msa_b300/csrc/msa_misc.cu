@@ -55,6 +55,39 @@ cudaError_t launch_merge_lse(const float* oa, const float* la, const float* ob, 
   return cudaGetLastError();
 }
 
+// Write-back: every (row, KV head, 16-byte piece) of the chunk's K and V moves to its
+// pool slot; one thread per piece, reads coalesced along the chunk row, writes along the
+// pool row.  A negative slot skips the row; a slot past the pool is ignored.
+__global__ void msa_kv_append_kernel(const int32_t* __restrict__ dst_slot, const uint4* __restrict__ kc,
+                                     const uint4* __restrict__ vc, uint4* __restrict__ kp, uint4* __restrict__ vp,
+                                     int64_t n, int Hkv, int d8, int64_t pool_slots) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t per_row = (int64_t)Hkv * d8;
+  if (idx >= n * per_row) return;
+  const int64_t row = idx / per_row;
+  const int rem = (int)(idx % per_row);
+  const int g = rem / d8, c = rem % d8;
+  const int64_t slot = dst_slot[row];
+  if (slot < 0 || slot >= pool_slots) return;
+  const int64_t blk = slot / kBlock, t = slot % kBlock;
+  const int64_t dst = ((blk * Hkv + g) * kBlock + t) * d8 + c;
+  kp[dst] = kc[idx];
+  vp[dst] = vc[idx];
+}
+
+cudaError_t launch_kv_append(const int32_t* dst_slot, const void* kc, const void* vc, void* kp, void* vp, int64_t n,
+                             int Hkv, int d, int64_t pool_blocks, cudaStream_t stream) {
+  const int d8 = d / 8;
+  const int64_t total = n * Hkv * d8;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  msa_kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+      dst_slot, reinterpret_cast<const uint4*>(kc), reinterpret_cast<const uint4*>(vc), reinterpret_cast<uint4*>(kp),
+      reinterpret_cast<uint4*>(vp), n, Hkv, d8, pool_blocks * kBlock);
+  return cudaGetLastError();
+}
+
 // Gather: one CTA per gather unit (a pool block or a run of consecutive chunk rows);
 // copies its tokens' K and V rows for every KV head with 16-byte moves.
 

@@ -641,3 +641,56 @@ extern "C" const char* msa_status_string(msa_status_t s) {
 }
 
 extern "C" int32_t msa_version(void) { return 1; }
+
+// ---------------------------------------------------------------- write-back placement
+// Rows of one sequence's chunk are grouped by position block (pos / 16); each group goes
+// to one pool block at offsets pos % 16, extending the block without a hole.  A group that
+// starts part-way into its position block continues the sequence's block holding it.
+extern "C" msa_status_t msa_append_plan(const int32_t* q_pos, int32_t n, const int32_t* free_blocks,
+                                        int32_t n_free, const int32_t* seq_blocks, int32_t n_seq_blocks,
+                                        int32_t* block_pos, int32_t* block_fill, int32_t num_pool_blocks,
+                                        int32_t* dst_slot, int32_t* new_blocks, int32_t* n_new) {
+  if (n < 0 || n_free < 0 || n_seq_blocks < 0 || num_pool_blocks < 0 || !n_new) return MSA_ERR_INVALID_ARG;
+  if (n > 0 && (!q_pos || !dst_slot || !block_pos || !block_fill)) return MSA_ERR_INVALID_ARG;
+  if (n_free > 0 && (!free_blocks || !new_blocks)) return MSA_ERR_INVALID_ARG;
+  if (n_seq_blocks > 0 && !seq_blocks) return MSA_ERR_INVALID_ARG;
+  *n_new = 0;
+  for (int32_t i = 0; i < n; ++i)
+    if (q_pos[i] < 0 || (i > 0 && q_pos[i] <= q_pos[i - 1])) return MSA_ERR_INVALID_ARG;
+  // first pass: validate and place, writing nothing
+  struct Group { int32_t blk, base, first_off, i0, i1; };
+  std::vector<Group> groups;
+  int32_t used = 0;
+  for (int32_t i = 0; i < n;) {
+    const int32_t base = q_pos[i] / kBlock * kBlock;
+    int32_t j = i;
+    while (j < n && q_pos[j] / kBlock * kBlock == base) ++j;
+    int32_t blk = -1, start = 0;
+    if (q_pos[i] % kBlock != 0) {
+      for (int32_t k = 0; k < n_seq_blocks; ++k) {
+        const int32_t b = seq_blocks[k];
+        if (b < 0 || b >= num_pool_blocks) return MSA_ERR_BLOCK_OOB;
+        if (block_fill[b] > 0 && block_pos[b] == base) blk = b;
+      }
+      if (blk < 0) return MSA_ERR_INVALID_ARG;
+      start = block_fill[blk];
+    } else {
+      if (used >= n_free) return MSA_ERR_WORKSPACE;
+      blk = free_blocks[used++];
+      if (blk < 0 || blk >= num_pool_blocks) return MSA_ERR_BLOCK_OOB;
+    }
+    for (int32_t r = i; r < j; ++r)
+      if (q_pos[r] - base != start + (r - i)) return MSA_ERR_INVALID_ARG;  // a hole
+    groups.push_back({blk, base, start, i, j});
+    i = j;
+  }
+  // second pass: write
+  for (const Group& gp : groups) {
+    for (int32_t r = gp.i0; r < gp.i1; ++r) dst_slot[r] = gp.blk * kBlock + (q_pos[r] - gp.base);
+    block_pos[gp.blk] = gp.base;
+    block_fill[gp.blk] = gp.first_off + (gp.i1 - gp.i0);
+  }
+  for (int32_t u = 0; u < used; ++u) new_blocks[u] = free_blocks[u];
+  *n_new = used;
+  return MSA_OK;
+}

@@ -259,3 +259,83 @@ def test_prefill_schedule_balance():
     sc = msa.Plan.from_layout(lay).export_schedule()
     load = np.bincount(sc[:, 0], weights=sc[:, 5])
     assert load.max() <= 1.04 * load.mean()
+
+
+# ----------------------------------------------------------------------------- write-back placement
+
+def _random_append_case(rng, nb=64):
+    """A sequence whose chunk holds recomputed blocks (whole) and a suffix that may start
+    inside a partially written block; returns (q_pos, block_pos, block_fill, free, cont)."""
+    pool = nb * 2
+    block_pos = np.zeros(pool, np.int32)
+    block_fill = np.zeros(pool, np.int32)
+    evicted = np.sort(rng.choice(nb, size=int(rng.integers(1, nb // 2)), replace=False))
+    pos = np.concatenate([np.arange(b * 16, b * 16 + 16) for b in evicted])
+    # the old context ends part-way into a cached block that the suffix continues
+    cont = -1
+    start = nb * 16 + int(rng.integers(0, 16))
+    if start % 16:
+        cont = int(rng.integers(0, pool))
+        block_pos[cont] = start // 16 * 16
+        block_fill[cont] = start % 16
+    suffix = np.arange(start, start + int(rng.integers(1, 80)))
+    q_pos = np.concatenate([pos, suffix]).astype(np.int32)
+    free = [b for b in rng.permutation(pool).tolist() if b != cont][:len(q_pos) // 16 + 3]
+    others = [b for b in rng.permutation(pool).tolist() if b != cont and b not in free][:5]
+    seq_blocks = others + ([cont] if cont >= 0 else [])
+    return q_pos, block_pos, block_fill, free, seq_blocks
+
+
+def test_append_plan_matches_oracle():
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        q_pos, bp, bf, free, sb = _random_append_case(rng)
+        bp_c, bf_c = bp.copy(), bf.copy()
+        dst, new = msa.append_plan(q_pos, free, bp_c, bf_c, seq_blocks=sb)
+        d2, n2, bp2, bf2 = O.append_plan(q_pos, free, bp, bf, seq_blocks=sb)
+        np.testing.assert_array_equal(dst, d2)
+        np.testing.assert_array_equal(new, n2)
+        np.testing.assert_array_equal(bp_c, bp2)
+        np.testing.assert_array_equal(bf_c, bf2)
+
+
+def test_append_plan_preserves_positions():
+    """Pinned independently of the placement rule: every row lands in a distinct slot whose
+    block position plus offset is the row's own position, inside the block's fill."""
+    rng = np.random.default_rng(12)
+    for _ in range(100):
+        q_pos, bp, bf, free, sb = _random_append_case(rng)
+        dst, new = msa.append_plan(q_pos, free, bp, bf, seq_blocks=sb)
+        assert len(set(dst.tolist())) == len(dst)
+        blk, off = dst // 16, dst % 16
+        np.testing.assert_array_equal(bp[blk] + off, q_pos)
+        assert np.all(off < bf[blk])
+        assert set(new.tolist()) <= set(free) and len(new) == len(set(blk.tolist()) - set(sb))
+
+
+def test_append_plan_errors():
+    bp = np.zeros(8, np.int32)
+    bf = np.zeros(8, np.int32)
+    with pytest.raises(msa.MSAError):                       # a hole inside a block
+        msa.append_plan([0, 1, 3], [0, 1], bp.copy(), bf.copy())
+    with pytest.raises(msa.MSAError):                       # unsorted positions
+        msa.append_plan([5, 4], [0, 1], bp.copy(), bf.copy())
+    with pytest.raises(msa.MSAError) as e:                  # not enough free blocks
+        msa.append_plan(list(range(40)), [0, 1], bp.copy(), bf.copy())
+    assert e.value.code == -5
+    with pytest.raises(msa.MSAError):                       # mid-block start without its block
+        msa.append_plan([20, 21], [0, 1], bp.copy(), bf.copy())
+    b2 = bp.copy(); f2 = bf.copy(); b2[3] = 16; f2[3] = 3
+    with pytest.raises(msa.MSAError):                       # continued block's fill disagrees
+        msa.append_plan([20, 21], [0, 1], b2, f2, seq_blocks=[3])
+    b4 = bp.copy(); f4 = bf.copy(); b4[3] = 16; f4[3] = 4
+    dst, new = msa.append_plan([20, 21, 32], [6], b4, f4, seq_blocks=[1, 3])   # continues block 3
+    assert dst.tolist() == [3 * 16 + 4, 3 * 16 + 5, 6 * 16] and new.tolist() == [6] and f4[3] == 6
+    with pytest.raises(msa.MSAError) as e:                  # block id outside the pool
+        msa.append_plan([0], [9], bp.copy(), bf.copy())
+    assert e.value.code == -4
+    # nothing was written by a failed call
+    b3 = bp.copy(); f3 = bf.copy()
+    with pytest.raises(msa.MSAError):
+        msa.append_plan([0, 1, 16, 18], [2, 5], b3, f3)
+    assert not b3.any() and not f3.any()
