@@ -284,6 +284,7 @@ def run_ours(args, world, rank, local):
     d2h_dc = hdout.numel() * hdout.element_size() + hdlse.numel() * hdlse.element_size()
 
     append = append_bench(msa, W, pl, pw, dev, flush)
+    ablation = ablation_bench(msa, W, pl, pw, dev, flush, pf_mean) if not args.no_ablation else None
 
     result = {
         "metric": METRIC,
@@ -326,6 +327,7 @@ def run_ours(args, world, rank, local):
                 "h2d_bytes_per_step": h2d_pf + h2d_dc, "d2h_bytes_per_step": d2h_pf + d2h_dc,
                 "prefill_ms": round(e2e_pf, 4), "decode_ms": round(e2e_dc, 4)},
         "append": append,
+        "ablation_per_segment": ablation,
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
         "wall_s": round(wall, 3),
@@ -375,6 +377,56 @@ def append_bench(msa, W, pl, pw, dev, flush, reps: int = 20):
     ms = statistics.median(ts)
     nbytes = 2 * 2 * n * pl.num_heads_kv * pl.head_dim * 2
     return {"rows": n, "bytes": nbytes, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+
+
+def ablation_bench(msa, W, pl, pw, dev, flush, one_ms, reps: int = 10):
+    """The many-launch way that one MSA launch replaces: one prefill per cached segment
+    (the chunk rows as queries only) plus one over the chunk's own keys, then pairwise
+    log-sum-exp merges (msa_merge_lse; the bf16 -> fp32 casts between merges are torch's).
+    Same workload, same outputs; not part of the step."""
+    import numpy as np
+    import torch
+    plans = []
+    for seg in pl.segments:
+        sub = W.Layout(**{**vars(pl), "segments": np.asarray([seg], np.int32)})
+        plans.append(msa.Plan.from_layout(sub, chunk_queries_only=True).upload(dev))
+    plans.append(msa.Plan.from_layout(W.Layout(**{**vars(pl), "segments": np.zeros((0, 3), np.int32)})).upload(dev))
+    outs = [(torch.empty_like(pw.q), torch.empty(pw.q.shape[:2], dtype=torch.float32, device=dev)) for _ in plans]
+
+    def run():
+        for pln, (o, l) in zip(plans, outs):
+            msa.prefill(pln, pw.q, pw.k_chunk, pw.v_chunk, pw.k_pool, pw.v_pool, out=o, lse=l)
+
+    def merge():
+        acc_o, acc_l = outs[0][0].float(), outs[0][1]
+        for o, l in outs[1:]:
+            mo, ml = msa.merge_lse(acc_o, acc_l, o.float(), l)
+            acc_o, acc_l = mo.float(), ml
+        return acc_o, acc_l
+
+    for _ in range(3):
+        run()
+        merge()
+    t_run, t_merge = [], []
+    for _ in range(reps):
+        flush.fill_(5)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        run()
+        e[1].record()
+        merge()
+        e[2].record()
+        torch.cuda.synchronize()
+        t_run.append(e[0].elapsed_time(e[1]))
+        t_merge.append(e[1].elapsed_time(e[2]))
+    for pln in plans:
+        if msa.get_status(pln) != 0:
+            raise RuntimeError("device error in the per-segment ablation")
+    ms_run, ms_merge = statistics.median(t_run), statistics.median(t_merge)
+    return {"segments": int(len(pl.segments)), "prefill_launches": len(plans), "merges": len(plans) - 1,
+            "ms_segment_launches": round(ms_run, 4), "ms_merges": round(ms_merge, 4),
+            "ms_total": round(ms_run + ms_merge, 4), "ms_one_msa_launch": round(one_ms, 4),
+            "one_launch_speedup": round((ms_run + ms_merge) / one_ms, 3)}
 
 
 def _single_kernel_result(args, world, pl, dl, pst, dst, pf_mean, dc_mean, peaks, peak_kind, clocks):
@@ -497,6 +549,7 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true", help="skip the per-segment launch comparison")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="time one kernel alone (for profiling captures); not the bench line")
     args = ap.parse_args(argv)

@@ -72,7 +72,12 @@ typedef struct {
   int32_t decode_min_ctas;    /* decode: target number of CTAs when automatic, 0 = 16 x SMs */
   int32_t prefill_ctas;       /* prefill: CTAs of the persistent launch the work is balanced
                                  over (one per SM), 0 = 148 (the B300's SM count) */
-  int32_t reserved[3];        /* must be 0 */
+  int32_t chunk_queries_only; /* prefill: 0 = the chunk's rows are queries AND keys (MSA);
+                                 1 = queries only: the KV context is the pool segments alone
+                                 (partial attention over a subset of the context, e.g. one
+                                 segment, for a log-sum-exp merge; a query that sees no key
+                                 gets O = 0 and LSE = -inf) */
+  int32_t reserved[2];        /* must be 0 */
 } msa_plan_opts_t;
 
 typedef struct msa_plan msa_plan_t;

@@ -84,12 +84,16 @@ def canonical_tokens(layout, s: int) -> np.ndarray:
     return arr
 
 
-def gather_by_position(layout, s: int, k_pool, v_pool, k_chunk, v_chunk, dtype=np.float64):
+def gather_by_position(layout, s: int, k_pool, v_pool, k_chunk, v_chunk, dtype=np.float64,
+                       chunk_keys: bool = True):
     """K and V of sequence ``s`` in ascending original position (bit-exact copies).
+    With ``chunk_keys=False`` the chunk's own rows are left out (pool segments only).
 
     Returns (pos [L], K [L, Hkv, d], V [L, Hkv, d]).
     """
     tok = canonical_tokens(layout, s)
+    if not chunk_keys:
+        tok = tok[tok[:, 0] == POOL]
     L = len(tok)
     Hkv, d = layout.num_heads_kv, layout.head_dim
     K = np.empty((L, Hkv, d), dtype)
@@ -146,12 +150,15 @@ def attention(q: np.ndarray, q_pos: np.ndarray, k: np.ndarray, v: np.ndarray,
 
 
 def prefill(layout, q, k_chunk, v_chunk, k_pool, v_pool, scale: float,
-            rows: Optional[np.ndarray] = None, dtype=np.float64, row_block: int = 1024):
+            rows: Optional[np.ndarray] = None, dtype=np.float64, row_block: int = 1024,
+            chunk_keys: bool = True):
     """MSA prefill: every chunk token attends over pool segments plus the chunk's own
     fresh K/V, causally by original position (section 4.1, abstract, Eq. 1).
 
     Inputs are numpy arrays of the bf16 values (any float dtype).  ``rows`` selects
-    global query rows to evaluate (all if None).  Returns (rows, O, LSE).
+    global query rows to evaluate (all if None).  ``chunk_keys=False`` computes the
+    partial attention over the pool segments alone (the chunk rows are queries only),
+    one of the parts a log-sum-exp merge combines.  Returns (rows, O, LSE).
     """
     total = layout.total_q
     rows = np.arange(total) if rows is None else np.asarray(rows, np.int64)
@@ -161,7 +168,7 @@ def prefill(layout, q, k_chunk, v_chunk, k_pool, v_pool, scale: float,
     seq_of = np.searchsorted(cu, rows, side="right") - 1
     for s in np.unique(seq_of):
         sel = np.nonzero(seq_of == s)[0]
-        kpos, K, V = gather_by_position(layout, int(s), k_pool, v_pool, k_chunk, v_chunk, dtype)
+        kpos, K, V = gather_by_position(layout, int(s), k_pool, v_pool, k_chunk, v_chunk, dtype, chunk_keys)
         for i in range(0, len(sel), row_block):
             part = sel[i:i + row_block]
             r = rows[part]

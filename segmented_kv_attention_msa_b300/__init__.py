@@ -35,7 +35,8 @@ class _Opts(ctypes.Structure):
     _fields_ = [("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("decode_split_blocks", ctypes.c_int32), ("decode_min_ctas", ctypes.c_int32),
-                ("prefill_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("prefill_ctas", ctypes.c_int32), ("chunk_queries_only", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 class _Stats(ctypes.Structure):
@@ -131,11 +132,12 @@ class Plan:
 
     def __init__(self, mode: str, num_heads_q: int, num_heads_kv: int, head_dim: int,
                  segments, block_table, block_pos, block_fill, cu_q, q_pos=None,
-                 decode_split_blocks: int = 0, decode_min_ctas: int = 0, prefill_ctas: int = 0):
+                 decode_split_blocks: int = 0, decode_min_ctas: int = 0, prefill_ctas: int = 0,
+                 chunk_queries_only: bool = False):
         self.mode = mode
         m = MSA_PREFILL if mode == "prefill" else MSA_DECODE
         opts = _Opts(num_heads_q, num_heads_kv, head_dim, 16, decode_split_blocks, decode_min_ctas,
-                     prefill_ctas)
+                     prefill_ctas, 1 if chunk_queries_only else 0)
         self._keep = [np.ascontiguousarray(np.asarray(x, np.int32)) for x in
                       (segments, block_table, block_pos, block_fill, cu_q,
                        q_pos if q_pos is not None else np.zeros(0, np.int32))]

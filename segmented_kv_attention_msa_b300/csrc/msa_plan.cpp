@@ -28,7 +28,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-msa_status_t build_units(const msa_plan_opts_t* /*opts*/, msa_mode_t mode, int32_t num_seqs,
+msa_status_t build_units(const msa_plan_opts_t* opts, msa_mode_t mode, int32_t num_seqs,
                          const msa_segment_t* segs, int32_t num_segs, const int32_t* block_table,
                          int32_t max_blocks, const int32_t* block_pos, const int32_t* block_fill,
                          int32_t num_pool_blocks, const int32_t* cu_q, const int32_t* q_pos,
@@ -64,7 +64,7 @@ msa_status_t build_units(const msa_plan_opts_t* /*opts*/, msa_mode_t mode, int32
     for (int32_t r = r0; r < r1; ++r) {
       if (q_pos[r] < 0) return MSA_ERR_INVALID_ARG;
       if (r > r0 && q_pos[r] <= q_pos[r - 1]) return MSA_ERR_INVALID_ARG;
-      units[s].push_back({q_pos[r], SRC_CHUNK, r, 1});
+      if (!opts->chunk_queries_only) units[s].push_back({q_pos[r], SRC_CHUNK, r, 1});
     }
   }
   for (int32_t s = 0; s < num_seqs; ++s) {
@@ -121,7 +121,16 @@ bool walk_items(const std::vector<std::vector<int64_t>>& pre, const std::vector<
   for (int32_t it : order) {
     const std::vector<int64_t>& w = pre[it];  // prefix sums of tile weights, w[0] = 0
     const int32_t n = (int32_t)w.size() - 1;
-    int32_t j = 0;  // an empty list (a query tile that sees nothing) makes no piece
+    if (n == 0) {  // a query tile that sees no key: one empty piece writes its rows
+      if (cap < kWPiece) {
+        if (++c >= ctas) return false;
+        cap = T;
+      }
+      if (cuts) cuts->push_back({it, 0, 0, c});
+      cap -= kWPiece;
+      continue;
+    }
+    int32_t j = 0;
     while (j < n) {
       const int64_t rest = w[n] - w[j] + kWPiece;
       if (rest <= cap) {
@@ -248,8 +257,9 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
     return MSA_ERR_INVALID_ARG;
   if (mode != MSA_PREFILL && mode != MSA_DECODE) return MSA_ERR_INVALID_ARG;
   if (num_segs > 0 && (!segs || !block_table || !block_pos || !block_fill)) return MSA_ERR_INVALID_ARG;
-  for (int i = 0; i < 3; ++i)
+  for (int i = 0; i < 2; ++i)
     if (opts->reserved[i] != 0) return MSA_ERR_INVALID_ARG;
+  if (opts->chunk_queries_only != 0 && opts->chunk_queries_only != 1) return MSA_ERR_INVALID_ARG;
   if (opts->prefill_ctas < 0) return MSA_ERR_INVALID_ARG;
   const int32_t Hq = opts->num_heads_q, Hkv = opts->num_heads_kv, d = opts->head_dim;
   if (Hq <= 0 || Hkv <= 0) return MSA_ERR_INVALID_ARG;

@@ -406,7 +406,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const WorkRec wk = p.work[w];
       const QTileRec qt = p.qt[wk.qt];
       const int n = wk.n;
-      if (n == 0) continue;
+      if (n == 0) {
+        // a query tile that sees no key (a plan whose chunk rows are queries only): O = 0,
+        // LSE = -inf; no other role takes part
+        if (t < p.hpc && r < qt.nrows) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(qt.row0 + r) * p.Hq + wk.h0 + t) * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          p.lse[(size_t)(qt.row0 + r) * p.Hq + wk.h0 + t] = -INFINITY;
+        }
+        continue;
+      }
       if (t >= p.hpc) {
         it += n;
         ++wi;

@@ -346,3 +346,43 @@ def test_prefill_split_sharp_logits():
         b = int(rng.integers(0, lay.num_pool_blocks))
         wl.k_pool[b, :, int(rng.integers(0, 16)), :] = wl.q[int(rng.integers(0, lay.total_q)), :1, :] * 4
     check_prefill(lay, wl=wl, plan_kw={"prefill_ctas": 64})
+
+
+def _with_segments(lay, segs):
+    return W.Layout(**{**vars(lay), "segments": np.asarray(segs, np.int32).reshape(-1, 3)})
+
+
+@pytest.mark.parametrize("seed", [41, 42])
+def test_prefill_queries_only_and_per_segment_merge(seed):
+    """Queries-only plans (KV = pool segments alone) match the oracle, including rows that
+    see no key of their segment (O = 0, LSE = -inf); one launch per segment plus one over
+    the chunk's own keys, merged by log-sum-exp on the GPU, matches the single MSA launch."""
+    rng = np.random.default_rng(seed)
+    spec = W.random_prefill_spec(rng, 70, 0.5, 150, 700)
+    lay = W.custom_prefill(8, 2, 128, [spec], seed=seed, qk_std=0.6)
+    wl = W.make_values(lay, device="cuda")
+    a = workload_arrays(wl)
+    sc = 1.0 / math.sqrt(128)
+    whole_o, whole_l = run_prefill(lay, wl)[1:]
+    parts = []
+    for seg in lay.segments:
+        sub = _with_segments(lay, [seg])
+        plan = msa.Plan.from_layout(sub, chunk_queries_only=True).upload("cuda")
+        o, l = msa.prefill(plan, wl.q, wl.k_chunk, wl.v_chunk, wl.k_pool, wl.v_pool)
+        torch.cuda.synchronize()
+        assert msa.get_status(plan) == 0
+        _, ro, rl = O.prefill(sub, a["q"], a["k_chunk"], a["v_chunk"], a["k_pool"], a["v_pool"], sc,
+                              chunk_keys=False)
+        assert_close(np64(o), ro, "queries-only out")
+        assert_close(np64(l), rl, "queries-only lse")
+        parts.append((o, l))
+    nothing = _with_segments(lay, [])
+    parts.append(run_prefill(nothing, wl)[1:])
+    assert any(torch.isinf(l).any() for _, l in parts[:-1])
+    acc_o, acc_l = parts[0][0].float().contiguous(), parts[0][1]
+    for o, l in parts[1:]:
+        mo, ml = msa.merge_lse(acc_o, acc_l, o.float().contiguous(), l)
+        acc_o, acc_l = mo.float().contiguous(), ml
+    torch.cuda.synchronize()
+    assert_close(np64(acc_o), np64(whole_o), "per-segment merged out")
+    assert_close(np64(acc_l), np64(whole_l), "per-segment merged lse")

@@ -250,6 +250,37 @@ def test_merge_of_disjoint_key_sets_equals_whole(seed):
     np.testing.assert_allclose(ml, whole_l, rtol=1e-12, atol=1e-13)
 
 
+def _layout_with_segments(lay, segs):
+    return W.Layout(**{**vars(lay), "segments": np.asarray(segs, np.int32).reshape(-1, 3)})
+
+
+@pytest.mark.parametrize("seed", [3, 4])
+def test_per_segment_parts_merge_to_msa(seed):
+    """The queries-only variant (KV = pool segments alone), one launch per segment plus one
+    over the chunk's own keys, merged by log-sum-exp, equals MSA over the whole context:
+    the one-launch result the method replaces many launches with (ablation baseline)."""
+    rng = np.random.default_rng(seed)
+    spec = W.random_prefill_spec(rng, 24, 0.5, 40, 150)
+    lay = W.custom_prefill(4, 2, 16, [spec], seed=seed, qk_std=0.7)
+    wl = W.make_values(lay)
+    a = {k: getattr(wl, k).float().numpy().astype(np.float64) for k in ("q", "k_chunk", "v_chunk", "k_pool", "v_pool")}
+    sc = 1.0 / 4.0
+    _, whole_o, whole_l = O.prefill(lay, a["q"], a["k_chunk"], a["v_chunk"], a["k_pool"], a["v_pool"], sc)
+    o_parts, l_parts = [], []
+    for seg in lay.segments:
+        _, o, l = O.prefill(_layout_with_segments(lay, [seg]), a["q"], a["k_chunk"], a["v_chunk"], a["k_pool"],
+                            a["v_pool"], sc, chunk_keys=False)
+        o_parts.append(o)
+        l_parts.append(l)
+    _, o, l = O.prefill(_layout_with_segments(lay, []), a["q"], a["k_chunk"], a["v_chunk"], a["k_pool"], a["v_pool"], sc)
+    o_parts.append(o)
+    l_parts.append(l)
+    assert any(np.isneginf(x).any() for x in l_parts[:-1])   # some query sees nothing of some segment
+    mo, ml = O.merge_lse(o_parts, l_parts)
+    np.testing.assert_allclose(mo, whole_o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(ml, whole_l, rtol=1e-12, atol=1e-13)
+
+
 def test_merge_edge_cases():
     o1 = np.ones((2, 4))
     o2 = 3 * np.ones((2, 4))
