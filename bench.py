@@ -429,6 +429,116 @@ def ablation_bench(msa, W, pl, pw, dev, flush, one_ms, reps: int = 10):
             "one_launch_speedup": round((ms_run + ms_merge) / one_ms, 3)}
 
 
+# ----------------------------------------------------------------------------- latency model (Eq. 5)
+
+def latency_model_terms(l1, q1, l2, q2):
+    """Regressors of the two-segment prefill latency model, in 16-token blocks.
+
+    The paper's Eq. 5 gives only the marginal cost of recomputing one more block,
+    T(l1, q1+1, l2-1, q2) - T(l1, q1, l2, q2) = k5 (l1 + 2 q1) + (k2 - k3 + k5).  The plainest
+    T that has exactly that difference (our reading: a request whose first segment is l1
+    cached blocks followed by q1 recomputed ones, and whose second segment is l2 cached blocks
+    followed by q2 new ones) is T = k0 + k1 l1 + k2 q1 + k3 l2 + k4 q2 + k5 q1 (l1 + q1):
+    the quadratic term is the attention of the recomputed blocks over the context before
+    them, the linear terms the per-block work."""
+    return [1.0, l1, q1, l2, q2, q1 * (l1 + q1)]
+
+
+def fit_latency_model(samples):
+    """Least-squares fit of k0..k5 to [(l1, q1, l2, q2, ms), ...]; returns (k, r2)."""
+    import numpy as np
+    A = np.array([latency_model_terms(*x[:4]) for x in samples], np.float64)
+    y = np.array([x[4] for x in samples], np.float64)
+    k, *_ = np.linalg.lstsq(A, y, rcond=None)
+    resid = y - A @ k
+    r2 = 1.0 - float(resid @ resid) / float(((y - y.mean()) ** 2).sum())
+    return k, r2
+
+
+def two_segment_layout(W, l1, q1, l2, q2, seed):
+    """One sequence, blocks of 16: [l1 cached][q1 recomputed][l2 cached][q2 new]; the chunk
+    is the q1 + q2 blocks (Llama-3-8B-shaped heads)."""
+    import numpy as np
+    B = 16
+    runs = []
+    if l1:
+        runs.append((0, l1 * B))
+    if l2:
+        runs.append(((l1 + q1) * B, l2 * B))
+    chunk = np.concatenate([np.arange(l1 * B, (l1 + q1) * B), np.arange((l1 + q1 + l2) * B, (l1 + q1 + l2 + q2) * B)])
+    return W.custom_prefill(32, 8, 128, [W.SeqSpec(runs, chunk)], seed=seed, qk_std=1.0 / np.sqrt(128.0))
+
+
+def run_sweep(args):
+    """Cached-ratio sweep (the paper's Fig. 13 measures MSA performance over the cached-token
+    ratio; its values are not given) and a fit of the two-segment latency model (Eq. 5) to
+    this kernel's timings on one B300.  Prints one JSON line (not the bench line)."""
+    import numpy as np
+    import torch
+    import segmented_kv_attention_msa_b300 as msa
+    from segmented_kv_attention_msa_b300 import build as B
+    from segmented_kv_attention_msa_b300 import workload as W
+    if not os.path.exists(msa.LIB_PATH):
+        B.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def time_layout(lay, reps=8):
+        wl = W.make_values(lay, device=dev)
+        plan = msa.Plan.from_layout(lay).upload(dev)
+        out = torch.empty_like(wl.q)
+        lse = torch.empty(wl.q.shape[:2], dtype=torch.float32, device=dev)
+        for _ in range(3):
+            msa.prefill(plan, wl.q, wl.k_chunk, wl.v_chunk, wl.k_pool, wl.v_pool, out=out, lse=lse)
+        ts = []
+        for _ in range(reps):
+            flush.fill_(7)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            msa.prefill(plan, wl.q, wl.k_chunk, wl.v_chunk, wl.k_pool, wl.v_pool, out=out, lse=lse)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        if msa.get_status(plan) != 0:
+            raise RuntimeError("device error in the sweep")
+        return statistics.median(ts), plan.stats()["useful_flops"]
+
+    # cached-ratio sweep: 16384-token context of 1024 blocks, a random fraction cached, plus
+    # 256 new tokens; the chunk is every evicted block and the new tokens (one launch)
+    rng = np.random.default_rng(13)
+    sweep = []
+    for ratio in (0.0, 0.25, 0.5, 0.75, 0.9):
+        cached = rng.random(1024) < ratio
+        R = int((~cached).sum()) * 16 + 256
+        runs_pool, chunk = W._split_recompute(~cached, 1024 * 16, 256, [R])
+        spec = W.SeqSpec(W._cached_runs_tokens(cached) + runs_pool, chunk)
+        lay = W.custom_prefill(32, 8, 128, [spec], seed=17, qk_std=1.0 / np.sqrt(128.0))
+        ms, fl = time_layout(lay)
+        sweep.append({"cached_ratio": ratio, "cached_blocks": int(cached.sum()), "chunk_tokens": int(lay.total_q),
+                      "segments": int(len(lay.segments)), "ms": round(ms, 4), "useful_tflops": round(fl / ms / 1e9, 1)})
+    base = sweep[0]["ms"]
+    for x in sweep:
+        x["speedup_vs_full_recompute"] = round(base / x["ms"], 3)
+
+    # latency model: a grid of two-segment requests (in blocks)
+    samples = []
+    for l1 in (0, 64, 256):
+        for q1 in (16, 64, 128):
+            for l2 in (0, 64, 256):
+                for q2 in (8, 32):
+                    lay = two_segment_layout(W, l1, q1, l2, q2, seed=l1 + q1 + l2 + q2)
+                    ms, _ = time_layout(lay, reps=5)
+                    samples.append((l1, q1, l2, q2, ms))
+    k, r2 = fit_latency_model(samples)
+    res = {"kind": "cached_ratio_sweep_and_latency_model", "gpu": torch.cuda.get_device_name(dev),
+           "sweep": sweep,
+           "latency_model": {"terms": "T = k0 + k1 l1 + k2 q1 + k3 l2 + k4 q2 + k5 q1 (l1 + q1), blocks of 16, ms",
+                             "k": [float(f"{x:.6g}") for x in k], "r2": round(r2, 4), "samples": len(samples),
+                             "delta_T_B": "k5 (l1 + 2 q1) + (k2 - k3 + k5)"}}
+    print(json.dumps(res), flush=True)
+
+
 def _single_kernel_result(args, world, pl, dl, pst, dst, pf_mean, dc_mean, peaks, peak_kind, clocks):
     """Result line of a one-kernel run (--only), used for profiling captures."""
     res = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "only": args.only,
@@ -550,12 +660,18 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true", help="skip the per-segment launch comparison")
+    ap.add_argument("--sweep", action="store_true",
+                    help="cached-ratio sweep and latency-model fit (prints its own JSON line, not the bench line)")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="time one kernel alone (for profiling captures); not the bench line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup()
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
+        return
     if args.impl == "reference":
         res = run_reference(args, world, rank)
     else:

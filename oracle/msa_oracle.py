@@ -40,7 +40,7 @@ from typing import Dict, List, Optional, Sequence, Tuple
 import numpy as np
 
 BLOCK = 16
-POOL, CHUNK = 0, 1
+POOL, CHUNK, MIXED = 0, 1, 2
 SKIP, FULL, PARTIAL = 0, 1, 2
 TILE_ROWS = 128          # tokens per KV tile and per query tile
 TILE_BLOCKS = TILE_ROWS // BLOCK
@@ -249,9 +249,12 @@ def canonical_plan(layout) -> np.ndarray:
       n_kt  x (seq, src, tok_begin, n_tok, minpos, maxpos)
       n_qt  x (seq, row0, nrows, minpos, maxpos)
       n_cls x class                    for each query tile, one per KV tile of its sequence
-    KV tiles: walk the sequence's units in position order; a tile holds units of one
-    source only, at most 8 pool blocks (128 rows) or 128 chunk tokens; a new tile
-    starts when the source changes or the tile is full.  Query tiles: the sequence's
+    KV tiles: the sequence's KV in position order is cut into units of at most 16 tokens
+    -- a pool block is one unit; a run of chunk tokens with no pool block between them is
+    cut front to back into units of 16 (the last may be shorter) -- and every 8
+    consecutive units make a tile, whatever their sources (src POOL or CHUNK when all
+    units are of that kind, else MIXED).  A tile's smallest and largest positions are
+    those of its first and last token.  Query tiles: the sequence's
     chunk rows cut every 128.  Class of (query tile, KV tile): SKIP when the query
     tile's largest position is below the KV tile's smallest; FULL when the query
     tile's smallest position is at least the KV tile's largest and the KV tile holds
@@ -268,22 +271,24 @@ def canonical_plan(layout) -> np.ndarray:
         if mode == 1:
             base += len(tok)
             continue
-        # kv tiles over units
-        seq_kts = []
-        cur = None   # [src, tok_begin, n_tok, minpos, maxpos, n_units]
-        t_index = base
+        # tile units: pool blocks, and runs of chunk tokens cut into pieces of <= 16
+        tunits = []   # [src, n_tok, minpos, maxpos]
         for (p0, src, idx, n) in units:
-            limit = TILE_BLOCKS if src == POOL else TILE_ROWS
-            if cur is None or cur[0] != src or cur[5] >= limit:
-                if cur is not None:
-                    seq_kts.append(cur)
-                cur = [src, t_index, 0, p0, p0, 0]
-            cur[2] += n
-            cur[4] = p0 + n - 1
-            cur[5] += 1
-            t_index += n
-        if cur is not None:
-            seq_kts.append(cur)
+            if src == CHUNK and tunits and tunits[-1][0] == CHUNK and tunits[-1][1] < BLOCK:
+                tunits[-1][1] += 1
+                tunits[-1][3] = p0
+            else:
+                tunits.append([src, n, p0, p0 + n - 1])
+        # kv tiles: 8 units each
+        seq_kts = []
+        t_index = base
+        for a in range(0, len(tunits), TILE_BLOCKS):
+            grp = tunits[a:a + TILE_BLOCKS]
+            srcs = {u[0] for u in grp}
+            src = srcs.pop() if len(srcs) == 1 else MIXED
+            ntok = sum(u[1] for u in grp)
+            seq_kts.append([src, t_index, ntok, grp[0][2], grp[-1][3]])
+            t_index += ntok
         for c in seq_kts:
             kts.append((s, c[0], c[1], c[2], c[3], c[4]))
         # q tiles

@@ -17,7 +17,7 @@ constexpr int kTileRows = 128;      // tokens per KV tile / rows per query tile
 constexpr int kTileBlocks = kTileRows / kBlock;
 constexpr int kStatusBytes = 256;   // workspace head: status word + scheduling counters
 
-enum { SRC_POOL = 0, SRC_CHUNK = 1 };
+enum { SRC_POOL = 0, SRC_CHUNK = 1, SRC_MIXED = 2 };
 enum { CLS_SKIP = 0, CLS_FULL = 1, CLS_PARTIAL = 2 };
 
 // Query tile: `nrows` consecutive chunk rows of one sequence starting at global row
@@ -26,8 +26,11 @@ struct QTileRec {
   int32_t seq, row0, nrows, minpos, maxpos, list_begin, list_count, pad;
 };
 
-// KV tile.  Chunk tile: chunk rows [row0, row0 + ntok).  Pool tile: nblk blocks
-// blk[i] whose tokens sit at positions bpos[i] + t, t < bfill[i]; tile row 16*i + t.
+// KV tile: nblk units of up to 16 rows, unit i at tile rows 16*i .. 16*i + 15.  A pool
+// unit is block blk[i] >= 0 whose tokens sit at positions bpos[i] + t, t < bfill[i]; a
+// chunk unit (blk[i] = -(r + 1)) is chunk rows r .. r + bfill[i] - 1, the first at
+// position bpos[i].  src is SRC_POOL or SRC_CHUNK when every unit is of that kind, else
+// SRC_MIXED; row0 is unused.
 struct KTileRec {
   int32_t src, ntok, row0, nblk, minpos, maxpos, full, pad;
   int32_t blk[kTileBlocks];

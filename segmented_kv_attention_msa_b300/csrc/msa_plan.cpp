@@ -81,9 +81,15 @@ msa_status_t build_units(const msa_plan_opts_t* opts, msa_mode_t mode, int32_t n
   return MSA_OK;
 }
 
+// A KV tile's unit: a pool block, or up to 16 chunk tokens that are consecutive in the
+// canonical order (and so consecutive chunk rows).  One 16-row TMA box each.
+struct TileUnit {
+  int32_t src, id, first_pos, n;  // id: physical block, or the first chunk row
+};
+
 struct KTileHost {
   int32_t seq, src, tok_begin, ntok, minpos, maxpos, nunits;
-  int32_t first_unit;
+  int32_t first_unit;  // into the flat TileUnit list
 };
 
 
@@ -305,26 +311,36 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
   std::vector<QTileRec> qts;
   std::vector<int32_t> cls;
   std::vector<int32_t> seq_kt_begin(num_seqs + 1, 0);
+  std::vector<TileUnit> tunits;
   if (mode == MSA_PREFILL) {
+    // KV tiles: the sequence's units in position order, 8 per tile, pool blocks and runs of
+    // chunk tokens alike (a run of consecutive chunk tokens is cut into units of <= 16), so
+    // a fragmented cache still gives full tiles
     for (int32_t s = 0; s < num_seqs; ++s) {
       seq_kt_begin[s] = (int32_t)kts.size();
-      int32_t t_index = seq_tok_begin[s];
-      KTileHost cur{};
-      bool open = false;
-      for (size_t ui = 0; ui < units[s].size(); ++ui) {
-        const Unit& u = units[s][ui];
-        int32_t limit = u.src == SRC_POOL ? kTileBlocks : kTileRows;
-        if (!open || cur.src != u.src || cur.nunits >= limit) {
-          if (open) kts.push_back(cur);
-          cur = KTileHost{s, u.src, t_index, 0, u.first_pos, u.first_pos, 0, (int32_t)ui};
-          open = true;
+      const size_t tu0 = tunits.size();
+      for (const Unit& u : units[s]) {
+        if (u.src == SRC_CHUNK && !tunits.empty() && tunits.size() > tu0 && tunits.back().src == SRC_CHUNK &&
+            tunits.back().n < kBlock && tunits.back().id + tunits.back().n == u.id) {
+          tunits.back().n += 1;
+        } else {
+          tunits.push_back({u.src, u.id, u.first_pos, u.n});
         }
-        cur.ntok += u.n;
-        cur.maxpos = u.first_pos + u.n - 1;
-        cur.nunits += 1;
-        t_index += u.n;
       }
-      if (open) kts.push_back(cur);
+      int32_t t_index = seq_tok_begin[s];
+      for (size_t a = tu0; a < tunits.size(); a += kTileBlocks) {
+        const size_t b = std::min(tunits.size(), a + kTileBlocks);
+        KTileHost t{s, tunits[a].src, t_index, 0, tunits[a].first_pos, 0, (int32_t)(b - a), (int32_t)a};
+        for (size_t i = a; i < b; ++i) {
+          if (tunits[i].src != t.src) t.src = SRC_MIXED;
+          t.ntok += tunits[i].n;
+        }
+        // the last unit's last token: a chunk unit's tokens need not be at consecutive positions
+        const TileUnit& lu = tunits[b - 1];
+        t.maxpos = lu.src == SRC_POOL ? lu.first_pos + lu.n - 1 : q_pos[lu.id + lu.n - 1];
+        t_index += t.ntok;
+        kts.push_back(t);
+      }
     }
     seq_kt_begin[num_seqs] = (int32_t)kts.size();
     for (int32_t s = 0; s < num_seqs; ++s) {
@@ -400,17 +416,12 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
       r.minpos = t.minpos;
       r.maxpos = t.maxpos;
       r.full = t.ntok == kTileRows;
-      if (t.src == SRC_CHUNK) {
-        r.row0 = units[t.seq][t.first_unit].id;
-        r.nblk = 0;
-      } else {
-        r.nblk = t.nunits;
-        for (int32_t i = 0; i < t.nunits; ++i) {
-          const Unit& u = units[t.seq][t.first_unit + i];
-          r.blk[i] = u.id;
-          r.bpos[i] = u.first_pos;
-          r.bfill[i] = u.n;
-        }
+      r.nblk = t.nunits;
+      for (int32_t i = 0; i < t.nunits; ++i) {
+        const TileUnit& u = tunits[t.first_unit + i];
+        r.blk[i] = u.src == SRC_POOL ? u.id : -(u.id + 1);
+        r.bpos[i] = u.first_pos;
+        r.bfill[i] = u.n;
       }
     }
     size_t ci = 0;

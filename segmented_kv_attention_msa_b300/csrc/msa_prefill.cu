@@ -55,7 +55,7 @@ static_assert(2 * 128 * kPfRegsSoftmax + 128 * kPfRegsOther <= kPfThreads * kPfL
 constexpr int kKStages = 3;            // K tiles in flight (a slot frees once its QK^T is done)
 constexpr int kVStages = 2;            // V tiles (a slot frees once its PV is done)
 constexpr int kSlabBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
-constexpr int kMaskInts = 20;          // mask record: base[8], nvalid[8], src, pad[3]
+constexpr int kMaskInts = 24;          // mask record: base[8], nvalid[8], src[8]
 
 // Shared memory: small items first (barriers, mask records), then the operand tiles on
 // a 1024-byte boundary (the 128-byte swizzle pattern repeats every 1024 bytes).
@@ -133,23 +133,26 @@ __device__ __forceinline__ TileRec load_tile_rec(const PrefillParams& p, const i
 }
 
 // Issue the TMA loads of one K or V tile (whole warp calls; lane 0 posts the byte
-// count, lanes 0-7 load one 16-row paged block each, or lane 0 the 128-row chunk box).
+// count, lane i < 8 loads the tile's unit i as one 16-row box: a paged pool block
+// (blk >= 0) or 16 chunk rows starting at row -blk-1 (blk < 0)).  A unit past the
+// tile's last one reads rows out of the pool map's range and arrives as zeros.
 template <int D>
 __device__ __forceinline__ void issue_kv_tile(const TileRec& rec, uint8_t* dst, uint64_t* bar,
                                               const CUtensorMap* tm_chunk, const CUtensorMap* tm_pool,
                                               int g, int Hkv, int pool_rows, int lane) {
   constexpr int kSlabs = D / 64;
-  const int src = rec.get(0), row0 = rec.get(2), nblk = rec.get(3);
+  const int nblk = rec.get(3);
   const int blk = rec.get(8 + (lane & 7));
   if (lane == 0) mbar_arrive_expect_tx(bar, 128 * D * 2);
   __syncwarp();
-  if (src == SRC_CHUNK) {
-    if (lane == 0)
-      for (int s = 0; s < kSlabs; ++s) tma_load_2d(dst + s * kSlabBytes, tm_chunk, bar, g * D + s * 64, row0);
-  } else if (lane < kTileBlocks) {
-    // a missing block reads an out-of-range row and arrives as zeros
-    const int y = (lane < nblk) ? (blk * Hkv + g) * kBlock : pool_rows;
-    for (int s = 0; s < kSlabs; ++s) tma_load_2d(dst + s * kSlabBytes + lane * 2048, tm_pool, bar, s * 64, y);
+  if (lane < kTileBlocks) {
+    uint8_t* d = dst + lane * 2048;
+    if (lane < nblk && blk < 0) {
+      for (int s = 0; s < kSlabs; ++s) tma_load_2d(d + s * kSlabBytes, tm_chunk, bar, g * D + s * 64, -blk - 1);
+    } else {
+      const int y = (lane < nblk) ? (blk * Hkv + g) * kBlock : pool_rows;
+      for (int s = 0; s < kSlabs; ++s) tma_load_2d(d + s * kSlabBytes, tm_pool, bar, s * 64, y);
+    }
   }
 }
 
@@ -286,20 +289,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!pf_wait_warp(&v_empty[vs], ((vit / kVStages) & 1) ^ 1, p, abort_flag)) goto vprod_done;
         issue_kv_tile<D>(cur, sV + vs * L::kTileBytes, &v_full[vs], &tm_vc, &tm_vp, wk.g, p.Hkv, p.pool_rows, lane);
         last_v[vs] = vit;
-        // mask record: per 16-row block i, the first key's position (pool) or chunk row
-        // (chunk) and the number of valid keys; chunk tiles are compared by row index
-        // (chunk rows of one sequence are in position order)
+        // mask record: per 16-row unit i, the first key's position (pool unit) or chunk
+        // row (chunk unit), its number of valid keys and its source; chunk units are
+        // compared by row index (chunk rows of one sequence are in position order)
         {
-          const int src = cur.get(0), ntok = cur.get(1), row0 = cur.get(2), nblk = cur.get(3);
+          const int nblk = cur.get(3);
           const int i = lane & 7;
-          const int bp = cur.get(16 + i), bf = cur.get(24 + i);
+          const int blk = cur.get(8 + i), bp = cur.get(16 + i), bf = cur.get(24 + i);
+          const bool chunk = i < nblk && blk < 0;
           int val = 0;
           if (lane < 8) {
-            val = (src == SRC_CHUNK) ? row0 + 16 * i : bp;
+            val = chunk ? -blk - 1 : bp;
           } else if (lane < 16) {
-            val = (src == SRC_CHUNK) ? min(max(ntok - 16 * i, 0), 16) : (i < nblk ? bf : 0);
-          } else if (lane == 16) {
-            val = src;
+            val = i < nblk ? bf : 0;
+          } else if (lane < 24) {
+            val = chunk ? SRC_CHUNK : SRC_POOL;
           }
           if (lane < kMaskInts) sMask[vs * kMaskInts + lane] = val;
           __syncwarp();
@@ -451,14 +455,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           // key (block b, slot u) is visible iff u < cut_b, cut_b = clamp(ref - base_b + 1, 0, nvalid_b)
           if (!pf_wait_warp(&m_full[vs], (it / kVStages) & 1, p, abort_flag)) goto softmax_done;
           const int4* mr = reinterpret_cast<const int4*>(sMask + vs * kMaskInts);
-          const int4 b0 = mr[0], b1 = mr[1], f0 = mr[2], f1 = mr[3], sx = mr[4];
-          const int ref = sx.x == SRC_CHUNK ? qrow : qp;
+          const int4 b0 = mr[0], b1 = mr[1], f0 = mr[2], f1 = mr[3], s0 = mr[4], s1 = mr[5];
           const int base[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
           const int nv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+          const int sr[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
           for (int b = 0; b < 8; ++b) {
             // ref - base + 1 cannot overflow: a row past the end uses INT_MAX only against
-            // bases >= 0, and then the cut is the block's valid count
+            // bases >= 0, and then the cut is the unit's valid count
+            const int ref = sr[b] == SRC_CHUNK ? qrow : qp;
             const int d = ref - base[b];
             const int cut = d < 0 ? 0 : (d >= nv[b] ? nv[b] : d + 1);
 #pragma unroll
@@ -657,15 +662,18 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const PrefillTensors
   CUtensorMap mq, mkc, mvc, mkp, mvp;
   const uint64_t pool_rows = (uint64_t)T.num_pool_blocks * p.Hkv * kBlock;
   if (!make_map(&mq, T.q, (uint64_t)p.Hq * D, T.total_q, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mkc, T.k_chunk, (uint64_t)p.Hkv * D, T.total_q, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mvc, T.v_chunk, (uint64_t)p.Hkv * D, T.total_q, 128)) return cudaErrorInvalidValue;
-  // an empty pool still needs a valid map: point it at the chunk tensor (never read)
+  if (!make_map(&mkc, T.k_chunk, (uint64_t)p.Hkv * D, T.total_q, 16)) return cudaErrorInvalidValue;
+  if (!make_map(&mvc, T.v_chunk, (uint64_t)p.Hkv * D, T.total_q, 16)) return cudaErrorInvalidValue;
+  // an empty pool still needs a valid map: point it at the chunk tensor; only rows past
+  // its end are ever read from it (the zero fill of a tile's missing units)
+  PrefillParams pp = p;
   if (pool_rows) {
     if (!make_map(&mkp, T.k_pool, D, pool_rows, 16)) return cudaErrorInvalidValue;
     if (!make_map(&mvp, T.v_pool, D, pool_rows, 16)) return cudaErrorInvalidValue;
   } else {
     if (!make_map(&mkp, T.k_chunk, D, (uint64_t)T.total_q * p.Hkv, 16)) return cudaErrorInvalidValue;
     if (!make_map(&mvp, T.v_chunk, D, (uint64_t)T.total_q * p.Hkv, 16)) return cudaErrorInvalidValue;
+    pp.pool_rows = (int32_t)(T.total_q * p.Hkv);
   }
   const int smem = PfLayout<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(msa_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -678,7 +686,7 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const PrefillTensors
 
   const int grid = p.n_ctas;  // the planner balanced the pieces over this many CTAs
   if (grid == 0) return cudaSuccess;
-  msa_prefill_kernel<D><<<grid, kPfThreads, smem, stream>>>(mq, mkc, mvc, mkp, mvp, p);
+  msa_prefill_kernel<D><<<grid, kPfThreads, smem, stream>>>(mq, mkc, mvc, mkp, mvp, pp);
   return cudaGetLastError();
 }
 

@@ -353,10 +353,11 @@ def hand_expected():
     toks += [(0, 7, t, 176 + t) for t in range(5)]
     toks += [(1, 16 + r, 0, 181 + r) for r in range(4)]
     toks += [(0, 0, t, 192 + t) for t in range(16)]
-    kts = [(0, 0, 0, 128, 0, 127), (0, 0, 128, 32, 128, 159), (0, 1, 160, 16, 160, 175),
-           (0, 0, 176, 5, 176, 180), (0, 1, 181, 4, 181, 184), (0, 0, 185, 16, 192, 207)]
+    # units: 8 pool blocks (0-127) | block 3, block 1, chunk rows 0-15, block 7 (5 tokens),
+    # chunk rows 16-19, block 0: one tile of 8 pool units, then one mixed tile of 6 units
+    kts = [(0, O.POOL, 0, 128, 0, 127), (0, O.MIXED, 128, 16 + 16 + 16 + 5 + 4 + 16, 128, 207)]
     qts = [(0, 0, 20, 160, 184)]
-    cls = [O.FULL, O.PARTIAL, O.PARTIAL, O.PARTIAL, O.PARTIAL, O.SKIP]
+    cls = [O.FULL, O.PARTIAL]
     head = [0, 1, len(toks), len(kts), len(qts), len(cls)]
     return np.array(head + [x for t in toks for x in t] + [x for t in kts for x in t]
                     + [x for t in qts for x in t] + cls, np.int32)
@@ -399,7 +400,11 @@ def test_canonical_plan_invariants(idx):
         qp = lay.q_pos[r0:r0 + nr]
         for (ks, src, tb, nt, kmin, kmax) in kts:
             kp = toks[tb:tb + nt, 3]
-            assert np.all(toks[tb:tb + nt, 0] == src)
+            if src == O.MIXED:
+                assert set(toks[tb:tb + nt, 0].tolist()) == {O.POOL, O.CHUNK}
+            else:
+                assert np.all(toks[tb:tb + nt, 0] == src)
+            assert kmin == kp[0] and kmax == kp[-1]
             vis = kp[None, :] <= qp[:, None]
             c = cls[ci]; ci += 1
             if not vis.any():
