@@ -515,8 +515,15 @@ def run_sweep(args):
         spec = W.SeqSpec(W._cached_runs_tokens(cached) + runs_pool, chunk)
         lay = W.custom_prefill(32, 8, 128, [spec], seed=17, qk_std=1.0 / np.sqrt(128.0))
         ms, fl = time_layout(lay)
+        # prefix-only reuse (a prefix cache): the cached blocks before the first evicted one
+        # are reused, everything after them is recomputed, in one launch
+        f = int(np.argmin(cached)) if not cached.all() else 1024
+        pspec = W.SeqSpec([(0, f * 16)] if f else [], np.arange(f * 16, 1024 * 16 + 256))
+        ms_pre, _ = time_layout(W.custom_prefill(32, 8, 128, [pspec], seed=17, qk_std=1.0 / np.sqrt(128.0)))
         sweep.append({"cached_ratio": ratio, "cached_blocks": int(cached.sum()), "chunk_tokens": int(lay.total_q),
-                      "segments": int(len(lay.segments)), "ms": round(ms, 4), "useful_tflops": round(fl / ms / 1e9, 1)})
+                      "segments": int(len(lay.segments)), "ms": round(ms, 4), "useful_tflops": round(fl / ms / 1e9, 1),
+                      "prefix_only_reused_blocks": f, "prefix_only_ms": round(ms_pre, 4),
+                      "speedup_vs_prefix_only": round(ms_pre / ms, 3)})
     base = sweep[0]["ms"]
     for x in sweep:
         x["speedup_vs_full_recompute"] = round(base / x["ms"], 3)
@@ -531,10 +538,13 @@ def run_sweep(args):
                     ms, _ = time_layout(lay, reps=5)
                     samples.append((l1, q1, l2, q2, ms))
     k, r2 = fit_latency_model(samples)
+    pred = [float(np.dot(latency_model_terms(*x[:4]), k)) for x in samples]
+    max_rel = max(abs(pv - x[4]) / x[4] for pv, x in zip(pred, samples))
     res = {"kind": "cached_ratio_sweep_and_latency_model", "gpu": torch.cuda.get_device_name(dev),
            "sweep": sweep,
            "latency_model": {"terms": "T = k0 + k1 l1 + k2 q1 + k3 l2 + k4 q2 + k5 q1 (l1 + q1), blocks of 16, ms",
                              "k": [float(f"{x:.6g}") for x in k], "r2": round(r2, 4), "samples": len(samples),
+                             "max_rel_err": round(max_rel, 4),
                              "delta_T_B": "k5 (l1 + 2 q1) + (k2 - k3 + k5)"}}
     print(json.dumps(res), flush=True)
 

@@ -37,6 +37,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "msa_device.cuh"
 #include "msa_kernels.h"
 #include "msa_tmap.h"
@@ -319,70 +321,104 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // descriptors of every operand buffer, built once; the k-step offsets add to the
-      // start-address field (addresses stay below 2^18, so the field never overflows)
-      uint64_t qd[2], kd[kKStages], vd[kVStages];
-      for (int t = 0; t < 2; ++t) qd[t] = smem_desc_sw128(smem_u32(sQ + t * L::kTileBytes), 16, 1024);
-      for (int s = 0; s < kKStages; ++s) kd[s] = smem_desc_sw128(smem_u32(sK + s * L::kTileBytes), 16, 1024);
-      for (int s = 0; s < kVStages; ++s) vd[s] = smem_desc_sw128(smem_u32(sV + s * L::kTileBytes), kSlabBytes, 1024);
+      // one descriptor per operand ring, built once.  Slot and k-step offsets add to the
+      // start-address field in the low word (addresses stay below 2^18, so the field never
+      // carries); the high word (stride, version, swizzle) is the same for Q, K and V.
+      // Plain arithmetic, not arrays indexed by slot: those would live in local memory.
+      constexpr uint32_t kTileDesc = (uint32_t)(L::kTileBytes >> 4);
+      const uint64_t qd0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint32_t desc_hi = (uint32_t)(qd0 >> 32);
+      const uint32_t q_lo = (uint32_t)qd0;
+      const uint32_t k_lo = (uint32_t)smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint32_t v_lo = (uint32_t)smem_desc_sw128(smem_u32(sV), kSlabBytes, 1024);
+      auto desc = [&](uint32_t lo) { return ((uint64_t)desc_hi << 32) | lo; };
       int it = 0, wi = 0, ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0;  // phase bits of the K and V rings at (ks, vs)
+      // (the empty asm keeps the compiler from hoisting all 16 descriptors of a block out
+      // of the loops: this warpgroup runs with 64 registers)
       auto issue_qk = [&](int t, int kslot) {
+        uint32_t qd = q_lo + (uint32_t)t * kTileDesc, kd = k_lo + (uint32_t)kslot * kTileDesc;
+        asm volatile("" : "+r"(qd), "+r"(kd));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = (uint64_t)((((kk >> 2) * kSlabBytes) + (kk & 3) * 32) >> 4);
-          umma_ss(tmem + t * 128, qd[t] + off, kd[kslot] + off, kIdescQK, kk > 0);
+          const uint32_t off = (uint32_t)((((kk >> 2) * kSlabBytes) + (kk & 3) * 32) >> 4);
+          umma_ss(tmem + t * 128, desc(qd + off), desc(kd + off), kIdescQK, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int vslot, bool acc) {
+        uint32_t vd = v_lo + (uint32_t)vslot * kTileDesc;
+        asm volatile("" : "+r"(vd));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vd[vslot] + (uint64_t)((kk * 2048) >> 4),
-                  kIdescPV, (acc || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc(vd + (uint32_t)((kk * 2048) >> 4)), kIdescPV,
+                  (acc || kk > 0) ? 1u : 0u);
       };
-      for (int w = cta_w0; w < cta_w1; ++w) {
-        const int n = p.work[w].n;
-        if (n == 0) continue;
-        if (!pf_wait(q_full, wi & 1, p, abort_flag)) goto mma_done;
-        if (!pf_wait(&k_full[ks], kph, p, abort_flag)) goto mma_done;
-        tc_fence_after();
-        for (int t = 0; t < p.hpc; ++t) {
-          issue_qk(t, ks);
-          umma_commit(&s_full[t]);
-        }
-        if (n == 1) umma_commit(q_empty);
-        if (++ks == kKStages) { ks = 0; kph ^= 1; }
-        for (int j = 0; j < n; ++j) {
-          const int cur = it + j;
-          const bool has_next = j + 1 < n;
-          for (int t = 0; t < p.hpc; ++t) {
-            if (!pf_wait(&p_full[t], cur & 1, p, abort_flag)) goto mma_done;
-            if (t == 0) {
-              if (j == 0 && !pf_wait(&o_free[0], (wi & 1) ^ 1, p, abort_flag)) goto mma_done;
-              if (!pf_wait(&v_full[vs], vph, p, abort_flag)) goto mma_done;
-              if (has_next && !pf_wait(&k_full[ks], kph, p, abort_flag)) goto mma_done;
-            } else if (j == 0 && !pf_wait(&o_free[t], (wi & 1) ^ 1, p, abort_flag)) {
-              goto mma_done;
-            }
-            tc_fence_after();
-            issue_pv(t, vs, j > 0);
-            if (has_next) {
-              issue_qk(t, ks);
-              umma_commit(&s_full[t]);
-            } else {
-              umma_commit(&o_full[t]);
-            }
+      // HPC (query heads per CTA) is a compile-time constant here so that the head loop
+      // unrolls: between two heads' GEMM blocks this thread does as little as possible,
+      // since it shares its scheduler with a busy softmax warp.
+      auto mma_loop = [&](auto hpc_c) {
+        constexpr int HPC = decltype(hpc_c)::value;
+        for (int w = cta_w0; w < cta_w1; ++w) {
+          const int n = p.work[w].n;
+          if (n == 0) continue;
+          if (!pf_wait(q_full, wi & 1, p, abort_flag)) return;
+          if (!pf_wait(&k_full[ks], kph, p, abort_flag)) return;
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < HPC; ++t) {
+            issue_qk(t, ks);
+            umma_commit(&s_full[t]);
           }
-          // the K and V slots are handed back by the last softmax group once it sees
-          // the S (or O) that these GEMMs produced: that commit covers every MMA above
-          if (has_next && ++ks == kKStages) { ks = 0; kph ^= 1; }
-          if (j + 2 == n) umma_commit(q_empty);
-          if (++vs == kVStages) { vs = 0; vph ^= 1; }
+          if (n == 1) umma_commit(q_empty);
+          if (++ks == kKStages) { ks = 0; kph ^= 1; }
+          bool v_ok = false, k_ok = false;  // V of tile j / K of tile j+1 already seen full
+          for (int j = 0; j < n; ++j) {
+            const int cur = it + j;
+            const bool has_next = j + 1 < n;
+            // ring slots (and phases) of the next tile's V and of the K after it
+            int vs2 = vs + 1, ks2 = ks + 1;
+            uint32_t vph2 = vph, kph2 = kph;
+            if (vs2 == kVStages) { vs2 = 0; vph2 ^= 1; }
+            if (ks2 == kKStages) { ks2 = 0; kph2 ^= 1; }
+#pragma unroll
+            for (int t = 0; t < HPC; ++t) {
+              if (!pf_wait(&p_full[t], cur & 1, p, abort_flag)) return;
+              if (t == 0) {
+                if (!v_ok && !pf_wait(&v_full[vs], vph, p, abort_flag)) return;
+                if (has_next && !k_ok && !pf_wait(&k_full[ks], kph, p, abort_flag)) return;
+              }
+              if (j == 0 && !pf_wait(&o_free[t], (wi & 1) ^ 1, p, abort_flag)) return;
+              tc_fence_after();
+              issue_pv(t, vs, j > 0);
+              if (t == HPC - 1) {
+                // while the pipe works through these products, look (without waiting)
+                // whether the next tile's V and the K after it have landed
+                v_ok = has_next && mbar_test_wait(&v_full[vs2], vph2);
+                k_ok = j + 2 < n && mbar_test_wait(&k_full[ks2], kph2);
+              }
+              if (has_next) {
+                issue_qk(t, ks);
+                umma_commit(&s_full[t]);
+              } else {
+                umma_commit(&o_full[t]);
+              }
+            }
+            // the K and V slots are handed back by the last softmax group once it sees
+            // the S (or O) that these GEMMs produced: that commit covers every MMA above
+            if (has_next) { ks = ks2; kph = kph2; }
+            if (j + 2 == n) umma_commit(q_empty);
+            vs = vs2;
+            vph = vph2;
+          }
+          it += n;
+          ++wi;
         }
-        it += n;
-        ++wi;
-      }
-    mma_done:
+      };
+      if (p.hpc == 2)
+        mma_loop(std::integral_constant<int, 2>{});
+      else
+        mma_loop(std::integral_constant<int, 1>{});
+      // every exit (done or aborted) waits for its MMAs in flight before TMEM is freed
       umma_commit(&drain[0]);
       mbar_wait(&drain[0], 0, 1000000000ull);
     }

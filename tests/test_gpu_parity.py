@@ -242,7 +242,8 @@ def _spec(pool_runs, chunk):
 
 
 @pytest.mark.parametrize("case", ["no_cache", "prefix_only", "one_token", "single_segment",
-                                  "partial_blocks", "ragged_multi", "future_blocks", "tiny_tiles"])
+                                  "partial_blocks", "ragged_multi", "future_blocks", "tiny_tiles",
+                                  "sparse_chunk", "fragmented"])
 @pytest.mark.parametrize("heads", [(32, 8, 128), (4, 4, 64), (6, 2, 128), (3, 3, 64)])
 def test_prefill_edge_cases(case, heads):
     Hq, Hkv, d = heads
@@ -263,6 +264,16 @@ def test_prefill_edge_cases(case, heads):
                                        int(rng.integers(1, 400))) for _ in range(5)]
     elif case == "future_blocks":
         specs = [_spec([(0, 128), (640, 512)], np.arange(128, 640))]
+    elif case == "sparse_chunk":
+        # chunk positions with gaps (held by neither side), so consecutive chunk rows of one
+        # 16-key unit are not consecutive positions; partial pool blocks between them
+        pool = [(0, 16), (64, 16), (128, 40)]
+        free = np.concatenate([np.arange(16, 64), np.arange(80, 128), np.arange(168, 700)])
+        specs = [_spec(pool, np.sort(rng.choice(free, 330, replace=False)))]
+    elif case == "fragmented":
+        # half of 96 blocks cached at random, everything else recomputed in this launch:
+        # most KV tiles mix pool blocks and chunk rows
+        specs = [W.random_prefill_spec(rng, 96, 0.5, 40), W.random_prefill_spec(rng, 30, 0.3, 7)]
     else:  # tiny_tiles: alternating single cached blocks and single chunk tokens
         runs = [(32 * i, 16) for i in range(20)]
         chunk = np.concatenate([np.arange(32 * i + 16, 32 * i + 17) for i in range(20)])
