@@ -105,8 +105,10 @@ typedef struct {
  *                                       their original positions, strictly ascending per
  *                                       sequence; decode: cu_q must be 0..num_seqs (one
  *                                       query per sequence), q_pos may be NULL.
- * Errors: INVALID_ARG, UNSUPPORTED, POS_OVERLAP (pool and chunk positions of one
- * sequence repeat), BLOCK_OOB.  On error *out is NULL. */
+ * Errors: INVALID_ARG, UNSUPPORTED (also: num_pool_blocks * Hkv * 16 or, in prefill,
+ * total query rows * Hkv above 2^31 - 1, since the kernels address the pool and the chunk
+ * by 32-bit TMA row coordinates), POS_OVERLAP (pool and chunk positions of one sequence
+ * repeat), BLOCK_OOB.  On error *out is NULL. */
 msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t mode, int32_t num_seqs,
                              const msa_segment_t* segs, int32_t num_segs,
                              const int32_t* block_table, int32_t max_blocks_per_seq,

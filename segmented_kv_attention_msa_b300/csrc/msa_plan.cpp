@@ -9,6 +9,7 @@
 // Large Language Model Serving", section 4.1 (a KV context of disjoint regions) and the
 // abstract (evicted blocks recomputed at their original positions; adaptive chunking).
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <new>
 #include <numeric>
@@ -272,6 +273,10 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
   if (Hq % Hkv != 0 || (d != 64 && d != 128) || opts->block_size != kBlock) return MSA_ERR_UNSUPPORTED;
   if (opts->decode_split_blocks < 0 || opts->decode_min_ctas < 0) return MSA_ERR_INVALID_ARG;
   if (mode == MSA_PREFILL && cu_q[num_seqs] > 0 && !q_pos) return MSA_ERR_INVALID_ARG;
+  // the kernels see the pool as [num_pool_blocks * Hkv * 16] rows and the chunk K/V as
+  // [total_q * Hkv] rows of one head each, addressed by 32-bit TMA coordinates
+  if ((int64_t)num_pool_blocks * Hkv * kBlock > INT32_MAX) return MSA_ERR_UNSUPPORTED;
+  if (mode == MSA_PREFILL && (int64_t)cu_q[num_seqs] * Hkv > INT32_MAX) return MSA_ERR_UNSUPPORTED;
 
   std::vector<std::vector<Unit>> units;
   msa_status_t st = build_units(opts, mode, num_seqs, segs, num_segs, block_table, max_blocks,

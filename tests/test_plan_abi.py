@@ -142,6 +142,26 @@ def test_unsupported_gqa():
     expect(-2, num_heads_q=3, num_heads_kv=2)
 
 
+def test_pool_rows_beyond_int32():
+    """The pool seen as [blocks * Hkv * 16] rows must fit 32-bit TMA coordinates: one block
+    more than that limit is refused, the limit itself is accepted."""
+    lay = base_layout()
+    hkv = 8  # planning does not look at K/V values; more heads keep the arrays small
+    limit = (2 ** 31 - 1) // (hkv * 16)
+    nb = len(lay.block_pos)
+    for n, ok in ((limit, True), (limit + 1, False)):
+        bp = np.zeros(n, np.int32)
+        bf = np.zeros(n, np.int32)
+        bp[:nb], bf[:nb] = lay.block_pos, lay.block_fill
+        kw = dict(block_pos=bp, block_fill=bf, num_heads_q=hkv, num_heads_kv=hkv)
+        if ok:
+            make(lay, **kw)
+        else:
+            with pytest.raises(msa.MSAError) as e:
+                make(lay, **kw)
+            assert e.value.code == -2
+
+
 def test_block_out_of_range():
     lay = base_layout()
     bt = lay.block_table.copy()
