@@ -50,9 +50,10 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_traffic(name: str, src_file: str):
+def kernel_traffic(name: str, src_file: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current source of the kernel (sha256 of its .cu file); otherwise None."""
+    current source of the kernel (sha256 of its .cu file) and applies to this workload;
+    otherwise None."""
     summ = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
     src = os.path.join(ROOT, "segmented_kv_attention_msa_b300", "csrc", src_file)
     try:
@@ -62,7 +63,7 @@ def kernel_traffic(name: str, src_file: str):
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if kv.get("source_sha256") != sha:
+        if kv.get("source_sha256") != sha or kv.get("applies_to") != workload:
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
@@ -313,12 +314,12 @@ def run_ours(args, world, rank, local):
             "parallelism": f"replicas x{world}",
         },
         "roofline": {"bound": "tensor", "achieved": round(pf_ach, 2), "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": round(pf_ach / tc_peak, 4), "traffic": kernel_traffic("prefill", "msa_prefill.cu"),
+                     "frac": round(pf_ach / tc_peak, 4), "traffic": kernel_traffic("prefill", "msa_prefill.cu", pl.name),
                      "kernel": "msa_prefill_kernel<128>", "peak_source": f"{peak_kind} bf16_tflops (burst)"},
         "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "ms": round(dc_mean, 4),
                    "roofline": {"bound": "hbm", "achieved": round(dc_ach, 1), "peak": hbm_peak, "unit": "GB/s",
                                 "frac": round(dc_ach / hbm_peak, 4),
-                                "traffic": kernel_traffic("decode", "msa_decode.cu"),
+                                "traffic": kernel_traffic("decode", "msa_decode.cu", dl.name),
                                 "kernel": "msa_decode_kernel<128,4>", "peak_source": f"{peak_kind} hbm_gbs"},
                    "e2e": {"value": round(dbytes / (e2e_dc * 1e-3) / 1e9, 1), "unit": "GB/s",
                            "h2d_bytes_per_step": h2d_dc, "d2h_bytes_per_step": d2h_dc}},
@@ -560,7 +561,7 @@ def _single_kernel_result(args, world, pl, dl, pst, dst, pf_mean, dc_mean, peaks
                     "config": {"workload": pl.name},
                     "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
-                                 "traffic": kernel_traffic("prefill", "msa_prefill.cu"),
+                                 "traffic": kernel_traffic("prefill", "msa_prefill.cu", pl.name),
                                  "peak_source": f"{peak_kind} bf16_tflops (burst)"}})
     else:
         ach = dst["algorithmic_bytes"] / (dc_mean * 1e-3) / 1e9
@@ -568,7 +569,7 @@ def _single_kernel_result(args, world, pl, dl, pst, dst, pf_mean, dc_mean, peaks
                     "config": {"workload": dl.name},
                     "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                  "frac": round(ach / peaks["hbm_gbs"], 4),
-                                 "traffic": kernel_traffic("decode", "msa_decode.cu"),
+                                 "traffic": kernel_traffic("decode", "msa_decode.cu", dl.name),
                                  "peak_source": f"{peak_kind} hbm_gbs"}})
     return res
 
