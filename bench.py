@@ -10,9 +10,11 @@ value        = useful prefill TFLOP/s (4 d Hq per visible query/key pair) over t
                prefill launches; the decode's algorithmic HBM GB/s is in "decode".
 roofline     = prefill kernel vs the measured dense bf16 peak; decode.roofline = decode
                kernel vs the measured HBM copy bandwidth.
-e2e          = the same metrics with the step's inputs copied from pinned host memory and
+e2e          = the same metrics with every step's inputs copied from pinned host memory and
                its results read back inside the timed region (the KV pool and the plan
-               stay resident: they are the cache).
+               stay resident: they are the cache).  Copies and kernels run on three
+               streams with two buffer sets, as a serving loop would overlap them; the
+               serial figure (one stream) is reported beside it.
 cpu_baseline = the CPU oracle timed on this host on a bounded sample of the same workload.
 
 `--impl reference` times the CPU oracle as the reference arm (there is no other
@@ -68,6 +70,46 @@ def kernel_traffic(name: str, src_file: str, workload: str):
         return float(kv["dram_bytes_per_launch"])
     except Exception:
         return None
+
+
+def pipelined_e2e(steps, h2d, run, d2h, flush, dev):
+    """Milliseconds per step of a stream of `steps` steps, each uploading its inputs
+    (h2d), flushing L2 and running its kernel (run) and reading its results back (d2h).
+    Uploads, kernels and read-backs go to three streams; two buffer sets (b = k % 2) let
+    step k+1's upload and step k-1's read-back overlap step k's kernel.  A buffer set is
+    reused only after the step that last used it is done with it."""
+    import torch
+    s_in, s_c, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_in, ev_c, ev_out = [], [], []
+    torch.cuda.synchronize()
+    start.record()
+    for s in (s_in, s_c, s_out):
+        s.wait_event(start)
+    for k in range(steps):
+        b = k & 1
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(ev_c[k - 2])    # the kernel of step k-2 has read set b
+            h2d(b)
+            ev_in.append(torch.cuda.Event())
+            ev_in[k].record(s_in)
+        with torch.cuda.stream(s_c):
+            s_c.wait_event(ev_in[k])
+            if k >= 2:
+                s_c.wait_event(ev_out[k - 2])   # the results of step k-2 were read back
+            flush.fill_(k & 0xFF)
+            run(b)
+            ev_c.append(torch.cuda.Event())
+            ev_c[k].record(s_c)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_c[k])
+            d2h(b)
+            ev_out.append(torch.cuda.Event())
+            ev_out[k].record(s_out)
+    end.record(s_out)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
 
 
 class ClockSampler:
@@ -250,39 +292,76 @@ def run_ours(args, world, rank, local):
     hq = pw.q.cpu().pin_memory()
     hkc = pw.k_chunk.cpu().pin_memory()
     hvc = pw.v_chunk.cpu().pin_memory()
-    hout = torch.empty(pout.shape, dtype=pout.dtype).pin_memory()
-    hlse = torch.empty(plse.shape, dtype=plse.dtype).pin_memory()
     hdq = dw.q.cpu().pin_memory()
-    hdout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
-    hdlse = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
-    dq_dev, kc_dev, vc_dev = torch.empty_like(pw.q), torch.empty_like(pw.k_chunk), torch.empty_like(pw.v_chunk)
-    ddq_dev = torch.empty_like(dw.q)
-    e2e_steps = max(1, min(args.steps, 10))
+    h2d_pf = sum(t.numel() * t.element_size() for t in (hq, hkc, hvc))
+    d2h_pf = pout.numel() * pout.element_size() + plse.numel() * plse.element_size()
+    h2d_dc = hdq.numel() * hdq.element_size()
+    d2h_dc = dout.numel() * dout.element_size() + dlse.numel() * dlse.element_size()
+    e2e_steps = max(1, min(args.steps, 20))
+
+    # serial: one stream, every copy in line with the kernel (context for the pipelined figure)
+    sq = [torch.empty_like(pw.q), torch.empty_like(pw.k_chunk), torch.empty_like(pw.v_chunk)]
+    sho = [torch.empty(pout.shape, dtype=pout.dtype).pin_memory(), torch.empty(plse.shape, dtype=plse.dtype).pin_memory()]
+    sdq = torch.empty_like(dw.q)
+    shd = [torch.empty(dout.shape, dtype=dout.dtype).pin_memory(), torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()]
     pe = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e2e_steps)]
     torch.cuda.synchronize()
     for k in range(e2e_steps):
         flush.fill_(k & 0xFF)
         pe[k][0].record()
-        dq_dev.copy_(hq, non_blocking=True)
-        kc_dev.copy_(hkc, non_blocking=True)
-        vc_dev.copy_(hvc, non_blocking=True)
-        msa.prefill(pplan, dq_dev, kc_dev, vc_dev, pw.k_pool, pw.v_pool, out=pout, lse=plse)
-        hout.copy_(pout, non_blocking=True)
-        hlse.copy_(plse, non_blocking=True)
+        for d, h in zip(sq, (hq, hkc, hvc)):
+            d.copy_(h, non_blocking=True)
+        msa.prefill(pplan, sq[0], sq[1], sq[2], pw.k_pool, pw.v_pool, out=pout, lse=plse)
+        sho[0].copy_(pout, non_blocking=True)
+        sho[1].copy_(plse, non_blocking=True)
         pe[k][1].record()
-        ddq_dev.copy_(hdq, non_blocking=True)
-        msa.decode(dplan, ddq_dev, dw.k_pool, dw.v_pool, out=dout, lse=dlse)
-        hdout.copy_(dout, non_blocking=True)
-        hdlse.copy_(dlse, non_blocking=True)
+        sdq.copy_(hdq, non_blocking=True)
+        msa.decode(dplan, sdq, dw.k_pool, dw.v_pool, out=dout, lse=dlse)
+        shd[0].copy_(dout, non_blocking=True)
+        shd[1].copy_(dlse, non_blocking=True)
         pe[k][2].record()
     torch.cuda.synchronize()
-    e2e_pf = statistics.mean(pe[k][0].elapsed_time(pe[k][1]) for k in range(e2e_steps))
-    e2e_dc = statistics.mean(pe[k][1].elapsed_time(pe[k][2]) for k in range(e2e_steps))
-    e2e_pf, e2e_dc = reduce_max([e2e_pf, e2e_dc], world, dev)
-    h2d_pf = sum(t.numel() * t.element_size() for t in (hq, hkc, hvc))
-    d2h_pf = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
-    h2d_dc = hdq.numel() * hdq.element_size()
-    d2h_dc = hdout.numel() * hdout.element_size() + hdlse.numel() * hdlse.element_size()
+    ser_pf = statistics.mean(pe[k][0].elapsed_time(pe[k][1]) for k in range(e2e_steps))
+    ser_dc = statistics.mean(pe[k][1].elapsed_time(pe[k][2]) for k in range(e2e_steps))
+
+    # pipelined: the same per-step copies and launches, on three streams with two buffer
+    # sets, so that step k+1's upload and step k-1's read-back overlap step k's kernel
+    pin = [[torch.empty_like(pw.q), torch.empty_like(pw.k_chunk), torch.empty_like(pw.v_chunk)] for _ in range(2)]
+    pres = [[torch.empty_like(pout), torch.empty_like(plse)] for _ in range(2)]
+    phost = [[torch.empty(pout.shape, dtype=pout.dtype).pin_memory(),
+              torch.empty(plse.shape, dtype=plse.dtype).pin_memory()] for _ in range(2)]
+
+    def pf_h2d(b):
+        for d, h in zip(pin[b], (hq, hkc, hvc)):
+            d.copy_(h, non_blocking=True)
+
+    def pf_run(b):
+        msa.prefill(pplan, pin[b][0], pin[b][1], pin[b][2], pw.k_pool, pw.v_pool, out=pres[b][0], lse=pres[b][1])
+
+    def pf_d2h(b):
+        for h, d in zip(phost[b], pres[b]):
+            h.copy_(d, non_blocking=True)
+
+    din = [torch.empty_like(dw.q) for _ in range(2)]
+    dres = [[torch.empty_like(dout), torch.empty_like(dlse)] for _ in range(2)]
+    dhost = [[torch.empty(dout.shape, dtype=dout.dtype).pin_memory(),
+              torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()] for _ in range(2)]
+
+    def dc_h2d(b):
+        din[b].copy_(hdq, non_blocking=True)
+
+    def dc_run(b):
+        msa.decode(dplan, din[b], dw.k_pool, dw.v_pool, out=dres[b][0], lse=dres[b][1])
+
+    def dc_d2h(b):
+        for h, d in zip(dhost[b], dres[b]):
+            h.copy_(d, non_blocking=True)
+
+    e2e_pf = pipelined_e2e(e2e_steps, pf_h2d, pf_run, pf_d2h, flush, dev)
+    e2e_dc = pipelined_e2e(e2e_steps, dc_h2d, dc_run, dc_d2h, flush, dev)
+    if msa.get_status(pplan) != 0 or msa.get_status(dplan) != 0:
+        raise RuntimeError("device error during the end-to-end steps")
+    e2e_pf, e2e_dc, ser_pf, ser_dc = reduce_max([e2e_pf, e2e_dc, ser_pf, ser_dc], world, dev)
 
     append = append_bench(msa, W, pl, pw, dev, flush)
     ablation = ablation_bench(msa, W, pl, pw, dev, flush, pf_mean) if not args.no_ablation else None
@@ -326,7 +405,11 @@ def run_ours(args, world, rank, local):
         "prefill_ms": round(pf_mean, 4),
         "e2e": {"value": round(flops * world / (e2e_pf * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d_pf + h2d_dc, "d2h_bytes_per_step": d2h_pf + d2h_dc,
-                "prefill_ms": round(e2e_pf, 4), "decode_ms": round(e2e_dc, 4)},
+                "prefill_ms": round(e2e_pf, 4), "decode_ms": round(e2e_dc, 4),
+                "pipeline": "per step: H2D of its inputs, L2 flush + kernel, D2H of its results; "
+                            "3 streams, 2 buffer sets; ms = whole run / steps",
+                "serial": {"value": round(flops * world / (ser_pf * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                           "prefill_ms": round(ser_pf, 4), "decode_ms": round(ser_dc, 4)}},
         "append": append,
         "ablation_per_segment": ablation,
         "clocks": clocks,
