@@ -17,8 +17,9 @@
  *
  * Conventions.
  *  - All tensors named "device" are device pointers owned by the caller.  The
- *    library never allocates device memory.  The library owns only the opaque host
- *    plan object.
+ *    library allocates no device memory at run time; it owns the opaque host plan
+ *    object and, for msa_decode_no_alloc only, one fixed 8 MiB device array that is
+ *    part of the loaded module.
  *  - Launch functions are asynchronous on the given stream; they return argument and
  *    launch errors at once.  Errors found on the device (a bounded wait that ran out)
  *    are written to the workspace status word and read by msa_get_status.
@@ -137,9 +138,12 @@ msa_status_t msa_workspace_init(void* workspace, size_t bytes, cudaStream_t stre
  *   n_tok x (src, id, offset, pos)     canonical KV order, each sequence in turn;
  *                                      src 0 = pool (id = physical block, offset = slot),
  *                                      src 1 = chunk (id = global query row, offset 0)
- *   n_kt  x (seq, src, tok_begin, n_tok, minpos, maxpos)   prefill KV tiles: units of one
- *                                      source in position order, <= 8 pool blocks or
- *                                      <= 128 chunk tokens; new tile on source change
+ *   n_kt  x (seq, src, tok_begin, n_tok, minpos, maxpos)   prefill KV tiles: the
+ *                                      sequence's keys in position order as units of <= 16
+ *                                      keys (a pool block, or <= 16 chunk rows that follow
+ *                                      each other with no pool block between them), 8 units
+ *                                      per tile; src 0 / 1 = all units pool / chunk,
+ *                                      2 = mixed
  *   n_qt  x (seq, row0, nrows, minpos, maxpos)             query tiles of 128 rows
  *   n_cls x class (0 SKIP, 1 FULL, 2 PARTIAL), per query tile, per KV tile of its sequence
  * Decode plans export the tokens only (n_kt = n_qt = n_cls = 0).
