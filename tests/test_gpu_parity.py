@@ -282,6 +282,39 @@ def test_prefill_edge_cases(case, heads):
     check_prefill(lay)
 
 
+@pytest.mark.parametrize("heads", [(4, 2, 64), (32, 8, 128)])
+def test_prefill_empty_sequences(heads):
+    """Sequences with no chunk rows between sequences that have some: rows of the others
+    are unaffected and nothing is written for the empty ones."""
+    from tests.test_plan_abi import empty_sequence_specs
+    Hq, Hkv, d = heads
+    lay = W.custom_prefill(Hq, Hkv, d, empty_sequence_specs(), seed=3, qk_std=1.0 / math.sqrt(d) * 3)
+    check_prefill(lay)
+
+
+def test_prefill_without_query_rows():
+    lay = W.custom_prefill(4, 2, 64, [W.SeqSpec([(0, 48)], np.array([], np.int64))], seed=3)
+    wl = W.make_values(lay, device="cuda")
+    plan = msa.Plan.from_layout(lay).upload("cuda")
+    out, lse = msa.prefill(plan, wl.q, wl.k_chunk, wl.v_chunk, wl.k_pool, wl.v_pool)
+    torch.cuda.synchronize()
+    assert out.shape[0] == 0 and lse.shape[0] == 0
+    assert msa.get_status(plan) == 0
+
+
+def test_zero_rows_merge_and_append():
+    o = torch.empty(0, 4, 64, dtype=torch.float32, device="cuda")
+    l = torch.empty(0, 4, dtype=torch.float32, device="cuda")
+    out, lse = msa.merge_lse(o, l, o, l)
+    assert out.shape == (0, 4, 64) and lse.shape == (0, 4)
+    kp = torch.zeros(2, 2, 16, 64, dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    none = torch.empty(0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    msa.kv_append(torch.empty(0, dtype=torch.int32, device="cuda"), none, none, kp, vp)
+    torch.cuda.synchronize()
+    assert int(kp.count_nonzero()) == 0 and int(vp.count_nonzero()) == 0
+
+
 def test_prefill_sharp_logits():
     rng = np.random.default_rng(5)
     spec = W.random_prefill_spec(rng, 64, 0.5, 200, 700)

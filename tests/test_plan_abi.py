@@ -142,6 +142,33 @@ def test_unsupported_gqa():
     expect(-2, num_heads_q=3, num_heads_kv=2)
 
 
+def empty_sequence_specs():
+    """Sequences with nothing to recompute between sequences that have chunk rows."""
+    return [W.SeqSpec([(0, 64)], np.arange(64, 100)), W.SeqSpec([(0, 48)], np.array([], np.int64)),
+            W.SeqSpec([], np.arange(0, 20)), W.SeqSpec([(16, 32)], np.array([], np.int64))]
+
+
+def test_plan_with_empty_sequences_matches_oracle():
+    lay = W.custom_prefill(4, 2, 64, empty_sequence_specs(), seed=3)
+    pl = msa.Plan.from_layout(lay)
+    assert np.array_equal(pl.export(), O.canonical_plan(lay))
+    sch = pl.export_schedule().reshape(-1, 9)
+    ex = pl.export()
+    n_tok, n_kt, n_qt = ex[2], ex[3], ex[4]
+    qts = ex[6 + 4 * n_tok + 6 * n_kt:][:5 * n_qt].reshape(-1, 5)
+    assert set(qts[:, 0].tolist()) == {0, 2}            # query tiles only where rows exist
+    assert set(sch[:, 1].tolist()) == set(range(n_qt))   # and every one is scheduled
+
+
+def test_plan_without_query_rows():
+    lay = W.custom_prefill(4, 2, 64, [W.SeqSpec([(0, 48)], np.array([], np.int64))], seed=3)
+    pl = msa.Plan.from_layout(lay)
+    st = pl.stats()
+    assert st["useful_flops"] == 0 and st["num_work_items"] == 0 and st["num_prefill_ctas"] == 0
+    assert np.array_equal(pl.export(), O.canonical_plan(lay))
+    assert pl.export_schedule().size == 0
+
+
 def test_pool_rows_beyond_int32():
     """The pool seen as [blocks * Hkv * 16] rows must fit 32-bit TMA coordinates: one block
     more than that limit is refused, the limit itself is accepted."""
