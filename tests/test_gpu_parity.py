@@ -133,7 +133,8 @@ def check_decode(lay, seqs=None, **plan_kw):
     return plan, out, lse
 
 
-@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 8, 128), (4, 2, 64), (16, 2, 128), (6, 3, 64)])
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 8, 128), (4, 2, 64), (16, 2, 128), (6, 3, 64),
+                                        (32, 2, 128), (8, 1, 64)])
 @pytest.mark.parametrize("split", [0, 1, 3])
 def test_decode_small(Hq, Hkv, d, split):
     rng = np.random.default_rng(Hq * 7 + d + split)
@@ -244,7 +245,7 @@ def _spec(pool_runs, chunk):
 @pytest.mark.parametrize("case", ["no_cache", "prefix_only", "one_token", "single_segment",
                                   "partial_blocks", "ragged_multi", "future_blocks", "tiny_tiles",
                                   "sparse_chunk", "fragmented"])
-@pytest.mark.parametrize("heads", [(32, 8, 128), (4, 4, 64), (6, 2, 128), (3, 3, 64)])
+@pytest.mark.parametrize("heads", [(32, 8, 128), (4, 4, 64), (6, 2, 128), (3, 3, 64), (32, 2, 128), (8, 1, 64)])
 def test_prefill_edge_cases(case, heads):
     Hq, Hkv, d = heads
     rng = np.random.default_rng(hash(case) % 1000)
