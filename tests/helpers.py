@@ -28,3 +28,10 @@ def workload_arrays(wl):
     """Oracle inputs: the bf16 values of the workload as fp64 numpy arrays."""
     return dict(q=np64(wl.q), k_chunk=np64(wl.k_chunk), v_chunk=np64(wl.v_chunk),
                 k_pool=np64(wl.k_pool), v_pool=np64(wl.v_pool))
+
+
+def empty_sequence_specs():
+    """Prefill sequences with nothing to recompute between sequences that have chunk rows."""
+    from segmented_kv_attention_msa_b300 import workload as W
+    return [W.SeqSpec([(0, 64)], np.arange(64, 100)), W.SeqSpec([(0, 48)], np.array([], np.int64)),
+            W.SeqSpec([], np.arange(0, 20)), W.SeqSpec([(16, 32)], np.array([], np.int64))]

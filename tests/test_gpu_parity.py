@@ -14,7 +14,7 @@ import segmented_kv_attention_msa_b300 as msa
 from segmented_kv_attention_msa_b300 import build as B
 from segmented_kv_attention_msa_b300 import workload as W
 from oracle import msa_oracle as O
-from tests.helpers import assert_close, np64, workload_arrays
+from tests.helpers import assert_close, empty_sequence_specs, np64, workload_arrays
 
 pytestmark = pytest.mark.gpu
 
@@ -287,7 +287,6 @@ def test_prefill_edge_cases(case, heads):
 def test_prefill_empty_sequences(heads):
     """Sequences with no chunk rows between sequences that have some: rows of the others
     are unaffected and nothing is written for the empty ones."""
-    from tests.test_plan_abi import empty_sequence_specs
     Hq, Hkv, d = heads
     lay = W.custom_prefill(Hq, Hkv, d, empty_sequence_specs(), seed=3, qk_std=1.0 / math.sqrt(d) * 3)
     check_prefill(lay)

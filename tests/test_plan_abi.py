@@ -13,6 +13,7 @@ import segmented_kv_attention_msa_b300 as msa
 from segmented_kv_attention_msa_b300 import build as B
 from segmented_kv_attention_msa_b300 import workload as W
 from oracle import msa_oracle as O
+from tests.helpers import empty_sequence_specs
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -140,12 +141,6 @@ def test_unsupported_head_dim():
 
 def test_unsupported_gqa():
     expect(-2, num_heads_q=3, num_heads_kv=2)
-
-
-def empty_sequence_specs():
-    """Sequences with nothing to recompute between sequences that have chunk rows."""
-    return [W.SeqSpec([(0, 64)], np.arange(64, 100)), W.SeqSpec([(0, 48)], np.array([], np.int64)),
-            W.SeqSpec([], np.arange(0, 20)), W.SeqSpec([(16, 32)], np.array([], np.int64))]
 
 
 def test_plan_with_empty_sequences_matches_oracle():
