@@ -52,10 +52,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_sha256(text: str) -> str:
+    """sha256 of a C++/CUDA source with its comments, trailing blanks and empty lines
+    removed: a change to the comments alone leaves it unchanged."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
+
+
 def kernel_traffic(name: str, src_file: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current source of the kernel (sha256 of its .cu file) and applies to this workload;
-    otherwise None."""
+    current code of the kernel (code_sha256 of its .cu file) and applies to this
+    workload; otherwise None."""
     summ = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
     src = os.path.join(ROOT, "segmented_kv_attention_msa_b300", "csrc", src_file)
     try:
@@ -64,8 +73,7 @@ def kernel_traffic(name: str, src_file: str, workload: str):
             if ":" in line:
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if kv.get("source_sha256") != sha or kv.get("applies_to") != workload:
+        if kv.get("code_sha256") != code_sha256(open(src).read()) or kv.get("applies_to") != workload:
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:

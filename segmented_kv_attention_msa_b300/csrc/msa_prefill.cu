@@ -10,20 +10,21 @@
 //
 // How (one persistent CTA per SM, warp-specialised, 12 warps in 3 warpgroups):
 //  * warp 10 (K producer): TMA loads of the Q tiles (two query heads sharing one KV head,
-//    128 chunk rows each) and of each K tile into a 3-deep ring.  A pool KV tile is 8
-//    paged blocks, one 16-row box per block and 64-column slab; a chunk KV tile is one
-//    128-row box per slab.  Missing blocks of a short pool tile are loaded from an
-//    out-of-range row and arrive as zeros.
+//    128 chunk rows each) and of each K tile into a 3-deep ring.  A KV tile is 8 units of
+//    at most 16 keys, each a paged pool block or a run of chunk rows, loaded as one
+//    16-row box per unit and 64-column slab; pool blocks and chunk rows may share a
+//    tile.  Missing units of a short tile are loaded from an out-of-range row and arrive
+//    as zeros.
 //  * warp 11 (V producer): the V tiles into a 2-deep ring, and for each tile a mask
-//    record (per 16-row block: the position or chunk row of its first key and its
+//    record (per unit: its source, the position or chunk row of its first key and its
 //    number of valid keys) used by partial tiles.
-//  * warp 8 (MMA issuer, one thread): tcgen05.mma kind::f16.  S_t = Q_t K^T (both
+//  * warp 8 (MMA issuer, one thread of it): tcgen05.mma kind::f16.  S_t = Q_t K^T (both
 //    operands in 128-byte-swizzled shared memory, accumulator in TMEM), then
 //    O_t += P_t V with P_t read from TMEM (it overwrites S_t as bf16) and V as an
 //    MN-major shared-memory operand.  The two heads ping-pong: while one softmax group
 //    works on S_0, the tensor core runs the other head's GEMMs.
 //  * warps 0-3 / 4-7 (softmax groups, one per head): each thread owns one query row in
-//    TMEM (tcgen05.ld 32x32b), masks partial tiles by a per-block prefix cut, takes the
+//    TMEM (tcgen05.ld 32x32b), masks partial tiles by a per-unit prefix cut, takes the
 //    exponentials against the running reference max while finding the tile max in the
 //    same pass (re-doing the pass only if the max grew by more than 2^8), writes P as
 //    bf16 back to TMEM, and at the end normalises O and stores bf16 rows and the LSE.
