@@ -79,6 +79,36 @@ def test_plan_random_layouts(seed):
     assert plan.stats()["useful_flops"] == O.useful_flops(lay)
 
 
+def sparse_spec(rng, nblocks):
+    """A sequence whose pool runs start on block boundaries and may end in a partial block,
+    and whose chunk holds random positions that no run holds (gaps anywhere), so chunk
+    units of consecutive rows have non-consecutive positions and tiles mix sources."""
+    runs, b = [], 0
+    taken = np.zeros(nblocks * 16, bool)
+    while b < nblocks:
+        if rng.random() < 0.5:
+            nb = min(int(rng.integers(1, 6)), nblocks - b)
+            ntok = nb * 16 - int(rng.integers(0, 16)) if rng.random() < 0.4 else nb * 16
+            runs.append((b * 16, ntok))
+            taken[b * 16:b * 16 + ntok] = True
+            b += nb
+        else:
+            b += int(rng.integers(1, 4))
+    free = np.nonzero(~taken)[0]
+    k = int(rng.integers(1, max(2, len(free))))
+    return W.SeqSpec(runs, np.sort(rng.choice(free, size=min(k, len(free)), replace=False)))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_plan_random_sparse_layouts(seed):
+    rng = np.random.default_rng(5000 + seed)
+    specs = [sparse_spec(rng, int(rng.integers(1, 30))) for _ in range(int(rng.integers(1, 5)))]
+    lay = W.custom_prefill(8, 2, 64, specs, seed=seed, shuffle_segments=True)
+    plan = msa.Plan.from_layout(lay)
+    np.testing.assert_array_equal(plan.export(), O.canonical_plan(lay))
+    assert plan.stats()["useful_flops"] == O.useful_flops(lay)
+
+
 def test_decode_plan_tokens_and_splits():
     lay = W.make_layout(4)
     plan = msa.Plan.from_layout(lay)
