@@ -461,7 +461,7 @@ def run_ours(args, world, rank, local):
                                   else "not flushed: each step reads more than L2 holds")}},
         "prefill_ms": round(pf_mean, 4),
         "e2e": {"value": round(flops * world / (e2e_pf * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d_pf + h2d_dc, "d2h_bytes_per_step": d2h_pf + d2h_dc,
+                "h2d_bytes_per_step": h2d_pf, "d2h_bytes_per_step": d2h_pf,
                 "prefill_ms": round(e2e_pf, 4), "decode_ms": round(e2e_dc, 4),
                 "pipeline": "per step: H2D of its inputs, L2 flush + kernel, D2H of its results; "
                             "3 streams, 2 buffer sets; ms = whole run / steps",
