@@ -152,6 +152,7 @@ class Plan:
         self.num_heads_q, self.num_heads_kv, self.head_dim = num_heads_q, num_heads_kv, head_dim
         self.num_seqs = num_seqs
         self.total_q = int(cq[-1])
+        self.num_pool_blocks = int(bp.shape[0])
         self.dev = None
         self.ws = None
 
@@ -220,6 +221,63 @@ class Plan:
         return self
 
 
+def _expect(t, shape, name, dtype=None, min_first=False):
+    """Raise ValueError unless tensor `t` has `shape` (with min_first: a first dimension of
+    at least shape[0]) and, if given, `dtype`.  The C ABI takes raw pointers and cannot
+    check sizes, so this is where a too-small tensor is caught before a kernel reads or
+    writes past its end."""
+    s = tuple(t.shape)
+    ok = len(s) == len(shape) and s[1:] == tuple(shape[1:]) and (
+        s[0] >= shape[0] if min_first else s[0] == shape[0])
+    if not ok:
+        need = ("at least " if min_first else "") + str(tuple(shape))
+        raise ValueError(f"{name} has shape {s}; the plan needs {need}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}; the plan needs {dtype}")
+
+
+def _check_pool(plan: "Plan", k_pool, v_pool):
+    shape = (plan.num_pool_blocks, plan.num_heads_kv, 16, plan.head_dim)
+    _expect(k_pool, shape, "k_pool", min_first=True)
+    _expect(v_pool, tuple(k_pool.shape), "v_pool")
+
+
+def _check_outputs(plan: "Plan", rows: int, out, lse):
+    import torch
+    _expect(out, (rows, plan.num_heads_q, plan.head_dim), "out", torch.bfloat16)
+    _expect(lse, (rows, plan.num_heads_q), "lse", torch.float32)
+    if not lse.is_contiguous():
+        raise ValueError("lse must be contiguous")
+
+
+def check_prefill_args(plan: "Plan", q, k_chunk, v_chunk, k_pool, v_pool, out=None, lse=None):
+    """Shapes and dtypes of a prefill call against its plan (no device access)."""
+    import torch
+    if plan.mode != "prefill":
+        raise ValueError("prefill needs a prefill plan")
+    T, Hq, Hkv, d = plan.total_q, plan.num_heads_q, plan.num_heads_kv, plan.head_dim
+    _expect(q, (T, Hq, d), "q", torch.bfloat16)
+    _expect(k_chunk, (T, Hkv, d), "k_chunk", torch.bfloat16)
+    _expect(v_chunk, (T, Hkv, d), "v_chunk", torch.bfloat16)
+    _check_pool(plan, k_pool, v_pool)
+    if out is not None or lse is not None:
+        _check_outputs(plan, T, out if out is not None else q, lse if lse is not None else
+                       torch.empty(T, Hq, dtype=torch.float32, device="meta"))
+
+
+def check_decode_args(plan: "Plan", q, k_pool, v_pool, out=None, lse=None):
+    """Shapes and dtypes of a decode call against its plan (no device access)."""
+    import torch
+    if plan.mode != "decode":
+        raise ValueError("decode needs a decode plan")
+    B, Hq, d = plan.num_seqs, plan.num_heads_q, plan.head_dim
+    _expect(q, (B, Hq, d), "q", torch.bfloat16)
+    _check_pool(plan, k_pool, v_pool)
+    if out is not None or lse is not None:
+        _check_outputs(plan, B, out if out is not None else q, lse if lse is not None else
+                       torch.empty(B, Hq, dtype=torch.float32, device="meta"))
+
+
 def _bf16(t, name):
     import torch
     if t is None:
@@ -235,6 +293,9 @@ def prefill(plan: Plan, q, k_chunk, v_chunk, k_pool, v_pool, out=None, lse=None,
     import torch
     for t, n in ((q, "q"), (k_chunk, "k_chunk"), (v_chunk, "v_chunk"), (k_pool, "k_pool"), (v_pool, "v_pool")):
         _bf16(t, n)
+    check_prefill_args(plan, q, k_chunk, v_chunk, k_pool, v_pool, out, lse)
+    if out is not None:
+        _bf16(out, "out")
     if plan.dev is None:
         plan.upload(q.device, stream)
     if out is None:
@@ -253,6 +314,9 @@ def decode(plan: Plan, q, k_pool, v_pool, out=None, lse=None, scale: Optional[fl
     import torch
     for t, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool")):
         _bf16(t, n)
+    check_decode_args(plan, q, k_pool, v_pool, out, lse)
+    if out is not None:
+        _bf16(out, "out")
     if plan.dev is None:
         plan.upload(q.device, stream)
     if out is None:
@@ -273,6 +337,14 @@ def merge_lse(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
     for t in (o_a, lse_a, o_b, lse_b):
         if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
             raise ValueError("merge_lse inputs must be contiguous fp32 CUDA tensors")
+    _expect(o_b, (rows, heads, d), "o_b")
+    _expect(lse_a, (rows, heads), "lse_a")
+    _expect(lse_b, (rows, heads), "lse_b")
+    if out is not None:
+        _bf16(out, "out")
+        _expect(out, (rows, heads, d), "out")
+    if lse is not None:
+        _expect(lse, (rows, heads), "lse", torch.float32)
     if out is None:
         out = torch.empty(rows, heads, d, dtype=torch.bfloat16, device=o_a.device)
     if lse is None:
@@ -285,6 +357,11 @@ def merge_lse(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
 def gather(plan: Plan, k_chunk, v_chunk, k_pool, v_pool, stream=None):
     """KV context of every sequence in canonical (position) order: (K, V, pos)."""
     import torch
+    _check_pool(plan, k_pool, v_pool)
+    if plan.mode == "prefill" and plan.total_q > 0:
+        for t, name in ((k_chunk, "k_chunk"), (v_chunk, "v_chunk")):
+            _bf16(t, name)
+            _expect(t, (plan.total_q, plan.num_heads_kv, plan.head_dim), name)
     n = plan.stats()["kv_tokens"]
     dev = k_pool.device
     if plan.dev is None:
@@ -326,6 +403,10 @@ def kv_append(dst_slot, k_chunk, v_chunk, k_pool, v_pool, stream=None):
     if dst_slot.dtype != torch.int32 or not dst_slot.is_cuda or not dst_slot.is_contiguous():
         raise ValueError("dst_slot must be a contiguous int32 CUDA tensor")
     n, hkv, d = k_chunk.shape
+    _expect(v_chunk, (n, hkv, d), "v_chunk")
+    _expect(k_pool, (k_pool.shape[0], hkv, 16, d) if k_pool.dim() == 4 else (0, hkv, 16, d), "k_pool")
+    _expect(v_pool, tuple(k_pool.shape), "v_pool")
+    _expect(dst_slot, (n,), "dst_slot")
     _check(lib().msa_kv_append(_dptr(dst_slot), _dptr(k_chunk), _dptr(v_chunk), _dptr(k_pool), _dptr(v_pool),
                                n, hkv, d, k_pool.shape[0], _stream(stream)), "msa_kv_append")
 
