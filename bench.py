@@ -1,15 +1,20 @@
 """Benchmark of the MSA hot path on B300.
 
-One step = one MSA prefill launch over the Llama-3-8B-shaped attention layer workload
-(32/8 heads, d = 128, 8192-token context in 16-token blocks, 60% cached in 3-10 runs,
-2048-token query chunk) followed by one MSA decode launch over the batch-64 decode
-workload (32/8 heads, contexts 4k-64k split into 2-32 scattered segments), both on
-inputs resident in HBM.  The plan (host planner) is built and uploaded before timing.
+One step = one MSA prefill launch over the largest prefill workload, the
+Llama-3-70B-shaped attention layer (64/8 heads, d = 128, 131072-token context in
+16-token blocks with >= 200 non-contiguous cached segments, 8192-token query chunk),
+followed by one MSA decode launch over the batch-64 decode workload (32/8 heads,
+contexts 4k-64k split into 2-32 scattered segments), both on inputs resident in HBM.
+The plan (host planner) is built and uploaded before timing.
 
 value        = useful prefill TFLOP/s (4 d Hq per visible query/key pair) over the timed
                prefill launches; the decode's algorithmic HBM GB/s is in "decode".
 roofline     = prefill kernel vs the measured dense bf16 peak; decode.roofline = decode
                kernel vs the measured HBM copy bandwidth.
+prefill_configs = every prefill workload of the metric (the Llama-3-8B-shaped layer with
+               an 8192-token context and 2048-token chunk, the 16-session multi-turn
+               batch, and the headline one), each timed alone the same way: ms, useful
+               TFLOP/s and the fraction of the measured peak.
 e2e          = the same metrics with every step's inputs copied from pinned host memory and
                its results read back inside the timed region (the KV pool and the plan
                stay resident: they are the cache).  Copies and kernels run on three
@@ -419,7 +424,18 @@ def run_ours(args, world, rank, local):
     e2e_pf, e2e_dc, ser_pf, ser_dc = reduce_max([e2e_pf, e2e_dc, ser_pf, ser_dc], world, dev)
 
     append = append_bench(msa, W, pl, pw, dev, flush)
-    ablation = ablation_bench(msa, W, pl, pw, dev, flush, pf_mean) if not args.no_ablation else None
+    configs = {}
+    for idx in PREFILL_WORKLOADS:
+        if idx == args.workload:
+            configs[pl.name] = prefill_entry(pl, pst, pf_mean, tc_peak, peak_kind)
+        else:
+            configs.update(time_prefill_workload(msa, W, idx, dev, flush, tc_peak, peak_kind, world))
+    ablation = None
+    if not args.no_ablation:
+        al = W.make_layout(2, tiler=msa.chunk_sizes)
+        aw = W.make_values(al, device=dev)
+        ablation = ablation_bench(msa, W, al, aw, dev, flush)
+        del aw
 
     result = {
         "metric": METRIC,
@@ -467,6 +483,7 @@ def run_ours(args, world, rank, local):
                             "3 streams, 2 buffer sets; ms = whole run / steps",
                 "serial": {"value": round(flops * world / (ser_pf * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                            "prefill_ms": round(ser_pf, 4), "decode_ms": round(ser_dc, 4)}},
+        "prefill_configs": configs,
         "append": append,
         "ablation_per_segment": ablation,
         "clocks": clocks,
@@ -476,6 +493,41 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(pl, pw, args.cpu_rows)
     return result
+
+
+PREFILL_WORKLOADS = (2, 3, 5)   # the prefill configurations of the metric (1 is the tiny parity case)
+
+
+def prefill_entry(pl, pst, ms, tc_peak, peak_kind):
+    ach = pst["useful_flops"] / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 4), "useful_tflops": round(ach, 2), "frac": round(ach / tc_peak, 4),
+            "peak_source": f"{peak_kind} bf16_tflops (burst)", "useful_flops": pst["useful_flops"],
+            "query_tokens": pl.total_q, "kv_tokens": pst["kv_tokens"], "segments": int(len(pl.segments)),
+            "traffic": kernel_traffic("prefill", "msa_prefill.cu", pl.name)}
+
+
+def time_prefill_workload(msa, W, idx, dev, flush, tc_peak, peak_kind, world, reps: int = 20):
+    """One prefill workload timed alone: warm-up, then `reps` launches each after an L2
+    flush, CUDA events on the launching stream, mean (max over ranks)."""
+    import torch
+    lay = W.make_layout(idx, tiler=msa.chunk_sizes)
+    wl = W.make_values(lay, device=dev)
+    plan = msa.Plan.from_layout(lay).upload(dev)
+    out = torch.empty_like(wl.q)
+    lse = torch.empty(wl.q.shape[:2], dtype=torch.float32, device=dev)
+    for _ in range(3):
+        msa.prefill(plan, wl.q, wl.k_chunk, wl.v_chunk, wl.k_pool, wl.v_pool, out=out, lse=lse)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in ev:
+        flush.fill_(9)
+        e0.record()
+        msa.prefill(plan, wl.q, wl.k_chunk, wl.v_chunk, wl.k_pool, wl.v_pool, out=out, lse=lse)
+        e1.record()
+    torch.cuda.synchronize()
+    if msa.get_status(plan) != 0:
+        raise RuntimeError(f"device error in prefill workload {idx}")
+    ms = reduce_max([statistics.mean(a.elapsed_time(b) for a, b in ev)], world, dev)[0]
+    return {lay.name: prefill_entry(lay, plan.stats(), ms, tc_peak, peak_kind)}
 
 
 def append_bench(msa, W, pl, pw, dev, flush, reps: int = 20):
@@ -520,13 +572,16 @@ def append_bench(msa, W, pl, pw, dev, flush, reps: int = 20):
     return {"rows": n, "bytes": nbytes, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
 
 
-def ablation_bench(msa, W, pl, pw, dev, flush, one_ms, reps: int = 10):
+def ablation_bench(msa, W, pl, pw, dev, flush, reps: int = 10):
     """The many-launch way that one MSA launch replaces: one prefill per cached segment
     (the chunk rows as queries only) plus one over the chunk's own keys, then pairwise
     log-sum-exp merges (msa_merge_lse; the bf16 -> fp32 casts between merges are torch's).
-    Same workload, same outputs; not part of the step."""
+    Same workload, same outputs, timed against one MSA launch; not part of the step."""
     import numpy as np
     import torch
+    one = msa.Plan.from_layout(pl).upload(dev)
+    one_out = torch.empty_like(pw.q)
+    one_lse = torch.empty(pw.q.shape[:2], dtype=torch.float32, device=dev)
     plans = []
     for seg in pl.segments:
         sub = W.Layout(**{**vars(pl), "segments": np.asarray([seg], np.int32)})
@@ -545,26 +600,37 @@ def ablation_bench(msa, W, pl, pw, dev, flush, one_ms, reps: int = 10):
             acc_o, acc_l = mo.float(), ml
         return acc_o, acc_l
 
+    def run_one():
+        msa.prefill(one, pw.q, pw.k_chunk, pw.v_chunk, pw.k_pool, pw.v_pool, out=one_out, lse=one_lse)
+
     for _ in range(3):
         run()
         merge()
-    t_run, t_merge = [], []
+        run_one()
+    t_run, t_merge, t_one = [], [], []
     for _ in range(reps):
         flush.fill_(5)
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         e[0].record()
         run()
         e[1].record()
         merge()
         e[2].record()
+        flush.fill_(6)
+        e[3].record()
+        run_one()
+        e[4].record()
         torch.cuda.synchronize()
         t_run.append(e[0].elapsed_time(e[1]))
         t_merge.append(e[1].elapsed_time(e[2]))
+        t_one.append(e[3].elapsed_time(e[4]))
+    one_ms = statistics.median(t_one)
     for pln in plans:
         if msa.get_status(pln) != 0:
             raise RuntimeError("device error in the per-segment ablation")
     ms_run, ms_merge = statistics.median(t_run), statistics.median(t_merge)
-    return {"segments": int(len(pl.segments)), "prefill_launches": len(plans), "merges": len(plans) - 1,
+    return {"workload": pl.name, "segments": int(len(pl.segments)), "prefill_launches": len(plans),
+            "merges": len(plans) - 1,
             "ms_segment_launches": round(ms_run, 4), "ms_merges": round(ms_merge, 4),
             "ms_total": round(ms_run + ms_merge, 4), "ms_one_msa_launch": round(one_ms, 4),
             "one_launch_speedup": round((ms_run + ms_merge) / one_ms, 3)}
@@ -750,12 +816,27 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def sample_rows(pl, n_rows, flop_budget, seed=0):
+    """Query rows for a bounded oracle run: `n_rows` random rows if n_rows > 0, else
+    random rows until their useful FLOPs reach `flop_budget`."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(pl.total_q)
+    if n_rows > 0:
+        return np.sort(order[:min(n_rows, pl.total_q)])
+    take, fl = 0, 0
+    while take < len(order) and fl < flop_budget:
+        step = max(1, min(len(order) - take, 8))
+        fl += sample_flops(pl, np.sort(order[take:take + step]))
+        take += step
+    return np.sort(order[:take])
+
+
 def cpu_baseline(pl, pw, n_rows):
     import numpy as np
     arrays = {k: getattr(pw, k).float().cpu().numpy().astype(np.float64)
               for k in ("q", "k_chunk", "v_chunk", "k_pool", "v_pool")}
-    rng = np.random.default_rng(0)
-    rows = np.sort(rng.choice(pl.total_q, min(n_rows, pl.total_q), replace=False))
+    rows = sample_rows(pl, n_rows, 6e11)
     secs = oracle_prefill_sample(pl, arrays, rows)
     fl = sample_flops(pl, rows)
     return {"value": round(fl / secs / 1e12, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
@@ -773,8 +854,7 @@ def run_reference(args, world, rank):
     pw = W.make_values(pl, device="cpu")
     arrays = {k: getattr(pw, k).float().numpy().astype(np.float64)
               for k in ("q", "k_chunk", "v_chunk", "k_pool", "v_pool")}
-    rng = np.random.default_rng(0)
-    rows = np.sort(rng.choice(pl.total_q, min(args.ref_rows, pl.total_q), replace=False))
+    rows = sample_rows(pl, args.ref_rows, 1e11)
     for _ in range(args.warmup):
         oracle_prefill_sample(pl, arrays, rows[:8])
     t = [oracle_prefill_sample(pl, arrays, rows) for _ in range(args.steps)]
@@ -803,12 +883,14 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=2, help="prefill workload (1, 2, 3 or 5)")
+    ap.add_argument("--workload", type=int, default=5, help="prefill workload (1, 2, 3 or 5)")
     ap.add_argument("--decode-workload", type=int, default=4)
     ap.add_argument("--decode-batch", type=int, default=64,
                     help="sequences of the decode workload (64 = the bench line; fewer for profiling captures)")
-    ap.add_argument("--cpu-rows", type=int, default=2048)
-    ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="query rows of the oracle baseline (0: as many as about 6e11 useful FLOPs)")
+    ap.add_argument("--ref-rows", type=int, default=0,
+                    help="query rows per reference-arm step (0: as many as about 1e11 useful FLOPs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true", help="skip the per-segment launch comparison")
     ap.add_argument("--sweep", action="store_true",

@@ -175,7 +175,8 @@ msa_status_t msa_chunk_sizes(int32_t R, int32_t min_chunk, int32_t max_chunk,
 /* MSA prefill (TTFT path), one launch for all sequences of the plan.
  *   q        device bf16 [total_q][Hq][d]
  *   k_chunk  device bf16 [total_q][Hkv][d], v_chunk likewise (the chunk's fresh K/V)
- *   k_pool   device bf16 [num_pool_blocks][Hkv][16][d], v_pool likewise
+ *   k_pool   device bf16 [num_pool_blocks][Hkv][16][d], v_pool likewise; slots past a
+ *            block's fill may hold anything (NaN and Inf included): they never reach a result
  *   out      device bf16 [total_q][Hq][d]; lse device fp32 [total_q][Hq]
  *   scale    softmax scale (1/sqrt(d) for Eq. 1)
  * All device pointers 16-byte aligned.  Errors: INVALID_ARG, MODE, WORKSPACE, CUDA. */
@@ -187,6 +188,7 @@ msa_status_t msa_prefill(const msa_plan_t* plan, const void* plan_dev,
 
 /* MSA decode (TPOT path): split-KV over the segments with the LSE merge fused in.
  *   q   device bf16 [num_seqs][Hq][d]; out bf16 [num_seqs][Hq][d]; lse fp32 [num_seqs][Hq]
+ *   k_pool, v_pool as for msa_prefill (slots past a block's fill may hold anything)
  * Errors: INVALID_ARG, MODE, WORKSPACE, CUDA. */
 msa_status_t msa_decode(const msa_plan_t* plan, const void* plan_dev, const void* q,
                         const void* k_pool, const void* v_pool,
@@ -203,14 +205,23 @@ msa_status_t msa_decode(const msa_plan_t* plan, const void* plan_dev, const void
  * process exits).  Plans whose msa_workspace_bytes exceed 8 MiB are rejected with
  * MSA_ERR_WORKSPACE.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture.  Each call clears the scratch's status word and merge counters on `stream`
- * (cudaMemsetAsync) and allocates nothing.  All calls share the one array, so calls that
- * may overlap on the GPU (other streams, other threads) race and must be serialised by the
- * caller.  Device-side errors of this variant stay in the library's scratch.
+ * capture.  The address is kept for the life of the process: do not use this entry point
+ * after a cudaDeviceReset (or anything else that destroys and re-creates the device's
+ * primary context), since the array is then re-loaded at another address.  Each call
+ * clears the scratch's status word and merge counters on `stream` (cudaMemsetAsync) and
+ * allocates nothing.  All calls share the one array, so calls that may overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller.  Its bounded
+ * waits use the limit of msa_set_wait_limit, like every other launch; a device-side error
+ * of this variant (a wait that ran out) is read with msa_get_status_no_alloc.
  * Errors: INVALID_ARG, MODE, WORKSPACE, CUDA. */
 msa_status_t msa_decode_no_alloc(const msa_plan_t* plan, const void* plan_dev, const void* q,
                                  const void* k_pool, const void* v_pool,
                                  void* out, float* lse, float scale, cudaStream_t stream);
+
+/* Synchronise `stream`, then read and clear the device status word that the last
+ * msa_decode_no_alloc call on the current device left in the library's scratch array.
+ * Returns MSA_OK or the device-side error (e.g. MSA_ERR_TIMEOUT); allocates nothing. */
+msa_status_t msa_get_status_no_alloc(cudaStream_t stream);
 
 /* Merge two partial attention results over disjoint key sets (elementwise over
  * rows x heads): m = max(lse_a, lse_b), w = exp(lse - m), O = (w_a O_a + w_b O_b)/(w_a + w_b),
@@ -270,6 +281,19 @@ msa_status_t msa_get_status(void* workspace, cudaStream_t stream);
  * spin before the kernel gives up with MSA_ERR_TIMEOUT; <= 0 restores the default of
  * 2 s.  Applies to later launches. */
 void msa_set_wait_limit(int64_t ns);
+
+/* Test hook for the give-up path (the paper has no counterpart).  Later launches of
+ * `kernel` leave out one of their copies, so that the bounded wait for it runs out and the
+ * kernel gives up exactly as it would on a copy that never completes: it records
+ * MSA_ERR_TIMEOUT in the status word, lets every copy and MMA it did start land, frees its
+ * tensor memory and returns.  kernel 0 = msa_prefill: CTA `cta` leaves out the K tile it
+ * would load as its `index`-th (counting from 0 over all its work); kernel 1 = msa_decode
+ * and msa_decode_no_alloc: warp 0 of CTA (split unit `cta`, head group 0) leaves out its
+ * `index`-th block.  Nothing faults and nothing waits past the wait limit.  Results of such
+ * a launch are undefined, and it may leave merge counters set: re-initialise the workspace
+ * (msa_workspace_init) before its next use.  A negative argument turns the hook off (the
+ * default). */
+void msa_set_test_drop(int32_t kernel, int32_t cta, int32_t index);
 
 const char* msa_status_string(msa_status_t status);
 int32_t msa_version(void);

@@ -71,12 +71,14 @@ EXPORTS = {
     "msa_prefill": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _SZ, _P]),
     "msa_decode": (_I32, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _SZ, _P]),
     "msa_decode_no_alloc": (_I32, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P]),
+    "msa_get_status_no_alloc": (_I32, [_P]),
     "msa_merge_lse": (_I32, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P]),
     "msa_gather": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "msa_append_plan": (_I32, [_P, _I32, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _I32P]),
     "msa_kv_append": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P]),
     "msa_get_status": (_I32, [_P, _P]),
     "msa_set_wait_limit": (None, [ctypes.c_int64]),
+    "msa_set_test_drop": (None, [_I32, _I32, _I32]),
     "msa_status_string": (ctypes.c_char_p, [_I32]),
     "msa_version": (_I32, []),
 }
@@ -418,3 +420,10 @@ def get_status(plan: Plan, stream=None) -> int:
 
 def set_wait_limit(ns: int):
     lib().msa_set_wait_limit(int(ns))
+
+
+def set_test_drop(kernel: str = None, cta: int = -1, index: int = -1):
+    """Test hook of the give-up path (msa_set_test_drop): later prefill or decode launches
+    leave out one copy so that the wait for it runs out.  No argument turns it off."""
+    k = {"prefill": 0, "decode": 1}.get(kernel, -1)
+    lib().msa_set_test_drop(k, int(cta), int(index))

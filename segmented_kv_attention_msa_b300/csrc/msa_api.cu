@@ -11,6 +11,8 @@ using namespace msa;
 namespace {
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s per wait
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+// test hook: which kernel leaves out a copy, in which CTA, and which copy (-1: none)
+std::atomic<int32_t> g_drop_kernel{-1}, g_drop_cta{-1}, g_drop_index{-1};
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -21,6 +23,22 @@ inline const T* at(const void* base, size_t off) {
 }  // namespace
 
 extern "C" void msa_set_wait_limit(int64_t ns) { g_wait_ns = ns > 0 ? (uint64_t)ns : kDefaultWaitNs; }
+
+extern "C" void msa_set_test_drop(int32_t kernel, int32_t cta, int32_t index) {
+  const bool on = (kernel == 0 || kernel == 1) && cta >= 0 && index >= 0;
+  g_drop_kernel = on ? kernel : -1;
+  g_drop_cta = on ? cta : -1;
+  g_drop_index = on ? index : -1;
+}
+
+namespace msa {
+uint64_t wait_limit_ns() { return g_wait_ns.load(); }
+void test_drop(int kernel, int32_t* cta, int32_t* index) {
+  const bool on = g_drop_kernel.load() == kernel;
+  *cta = on ? g_drop_cta.load() : -1;
+  *index = on ? g_drop_index.load() : -1;
+}
+}  // namespace msa
 
 extern "C" msa_status_t msa_plan_upload(const msa_plan_t* plan, void* plan_dev, size_t bytes,
                                         cudaStream_t stream) {
@@ -86,6 +104,7 @@ extern "C" msa_status_t msa_prefill(const msa_plan_t* plan, const void* plan_dev
   p.pool_rows = (int32_t)(pool_blocks * plan->Hkv * kBlock);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = g_wait_ns.load();
+  test_drop(0, &p.drop_cta, &p.drop_k);
   PrefillTensors T{q, k_chunk, v_chunk, k_pool, v_pool, plan->total_q, pool_blocks, plan->d};
   return launch_prefill(p, T, stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
@@ -121,6 +140,7 @@ extern "C" msa_status_t msa_decode(const msa_plan_t* plan, const void* plan_dev,
   p.pool_rows = (int64_t)plan->num_pool_blocks * plan->Hkv * kBlock;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = g_wait_ns.load();
+  test_drop(1, &p.drop_split, &p.drop_k);
   return launch_decode(p, plan->d, plan->n_split, stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

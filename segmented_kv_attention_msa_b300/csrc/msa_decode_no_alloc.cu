@@ -92,6 +92,22 @@ extern "C" msa_status_t msa_decode_no_alloc(const msa_plan_t* plan, const void* 
   p.G = plan->G;
   p.pool_rows = (int64_t)plan->num_pool_blocks * plan->Hkv * kBlock;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.wait_ns = 2000000000ull;
+  p.wait_ns = wait_limit_ns();  // the same bound as every other launch (msa_set_wait_limit)
+  test_drop(1, &p.drop_split, &p.drop_k);
   return launch_decode(p, plan->d, plan->n_split, stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+// The status word sits at the start of the library's scratch array (offset 0 of the
+// workspace layout).  Reading it needs no allocation either: a copy into a host int.
+extern "C" msa_status_t msa_get_status_no_alloc(cudaStream_t stream) {
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return MSA_ERR_CUDA;
+  int32_t word = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MSA_ERR_CUDA;
+  if (word != 0) {
+    const int32_t zero = 0;
+    if (cudaMemcpy(scratch, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MSA_ERR_CUDA;
+  }
+  return (msa_status_t)word;
 }

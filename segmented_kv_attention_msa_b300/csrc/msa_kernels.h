@@ -24,6 +24,7 @@ struct PrefillParams {
   int32_t pool_rows;  // rows of the pool tensor maps; a box starting here reads zeros
   float scale_log2;
   uint64_t wait_ns;
+  int32_t drop_cta, drop_k;  // test hook: CTA drop_cta leaves out its K tile number drop_k (-1: none)
 };
 
 struct PrefillTensors {
@@ -49,6 +50,7 @@ struct DecodeParams {
   int64_t pool_rows;  // rows of the pool tensors seen as [num_blocks * Hkv * 16][d]
   float scale_log2;
   uint64_t wait_ns;
+  int32_t drop_split, drop_k;  // test hook: warp 0 of CTA (drop_split, 0) leaves out its block drop_k (-1: none)
 };
 
 struct GatherParams {
@@ -64,6 +66,11 @@ struct GatherParams {
   int32_t Hkv;
   int32_t d;
 };
+
+// Settings shared by every launch (set through the C ABI): the bound of each device wait
+// and the test hook that leaves out one copy (kernel 0 = prefill, 1 = decode).
+uint64_t wait_limit_ns();
+void test_drop(int kernel, int32_t* cta, int32_t* index);
 
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillTensors& T, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int d, int n_split, cudaStream_t stream);

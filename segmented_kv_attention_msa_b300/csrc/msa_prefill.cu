@@ -65,7 +65,7 @@ constexpr int kMaskInts = 24;          // mask record: base[8], nvalid[8], src[8
 template <int D>
 struct PfLayout {
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kNumBars = 28;
+  static constexpr int kNumBars = 29;
   static constexpr int kBar = 0;
   static constexpr int kMisc = (kBar + kNumBars * 8 + 15) / 16 * 16;  // TMEM base address, flags
   static constexpr int kMask = kMisc + 16;                             // int32 [kVStages][kMaskInts]
@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* drain = bars + 22;    // [2] one per MMA-issuing thread
   uint64_t* ep_bar = bars + 24;    // [2] split pieces: the head's 128 threads stored their partial
   uint64_t* ep_flag = bars + 26;   // [2] split pieces: merge counter read, last_flag[t] valid
+  uint64_t* v_land = bars + 28;    // V tiles with unused pool slots: the copy landed (then fixed up)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + L::kMisc + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem_raw + L::kMisc + 8);  // [2]
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
+    mbar_init(v_land, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -262,8 +264,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (j + 1 < n) nxt = load_tile_rec(p, lst, j + 1, lane);
         const int ks = kit % kKStages;
         if (!pf_wait_warp(&k_empty[ks], ((kit / kKStages) & 1) ^ 1, p, abort_flag)) goto kprod_done;
-        issue_kv_tile<D>(cur, sK + ks * L::kTileBytes, &k_full[ks], &tm_kc, &tm_kp, wk.g, p.Hkv, p.pool_rows, lane);
-        last_k[ks] = kit;
+        // (test hook: one CTA may leave out one K tile, so that the wait for it runs out)
+        if (!(kit == p.drop_k && (int)blockIdx.x == p.drop_cta)) {
+          issue_kv_tile<D>(cur, sK + ks * L::kTileBytes, &k_full[ks], &tm_kc, &tm_kp, wk.g, p.Hkv, p.pool_rows,
+                           lane);
+          last_k[ks] = kit;
+        }
         ++kit;
         cur = nxt;
       }
@@ -278,6 +284,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ------------------------------------------------------------ V producer (and mask records)
     int vit = 0;
     int last_v[kVStages] = {-1, -1};
+    int nfix = 0;               // V tiles whose copy landed on v_land
+    bool land_pending = false;  // a copy on v_land has not been seen to land
     for (int w = cta_w0; w < cta_w1; ++w) {
       const WorkRec wk = p.work[w];
       const QTileRec qt = p.qt[wk.qt];
@@ -290,7 +298,39 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (j + 1 < n) nxt = load_tile_rec(p, lst, j + 1, lane);
         const int vs = vit % kVStages;
         if (!pf_wait_warp(&v_empty[vs], ((vit / kVStages) & 1) ^ 1, p, abort_flag)) goto vprod_done;
-        issue_kv_tile<D>(cur, sV + vs * L::kTileBytes, &v_full[vs], &tm_vc, &tm_vp, wk.g, p.Hkv, p.pool_rows, lane);
+        {
+          // Pool units with unused slots (fill < 16): those slots may hold anything, NaN
+          // included, and P.V spans the unit's 16 rows.  A masked key has P = 0, but
+          // 0 x NaN is NaN, so their V rows are zeroed in shared memory before the MMA
+          // reads the tile: the copy lands on v_land, this warp clears the rows, and only
+          // then marks the slot full.  (Their K rows need nothing: the mask replaces
+          // those logits by -inf.)
+          uint8_t* vdst = sV + vs * L::kTileBytes;
+          const int ui = lane & 7;
+          const int u_n = cur.get(3), u_blk = cur.get(8 + ui), u_fill = cur.get(24 + ui);  // all lanes
+          const bool fix_u = lane < kTileBlocks && ui < u_n && u_blk >= 0 && u_fill < kBlock;
+          const unsigned fixmask = __ballot_sync(0xffffffffu, fix_u);
+          if (fixmask == 0) {
+            issue_kv_tile<D>(cur, vdst, &v_full[vs], &tm_vc, &tm_vp, wk.g, p.Hkv, p.pool_rows, lane);
+          } else {
+            issue_kv_tile<D>(cur, vdst, v_land, &tm_vc, &tm_vp, wk.g, p.Hkv, p.pool_rows, lane);
+            land_pending = true;
+            if (!pf_wait_warp(v_land, nfix & 1, p, abort_flag)) goto vprod_done;
+            land_pending = false;
+            ++nfix;
+            for (int i = 0; i < kTileBlocks; ++i) {
+              const int f = cur.get(24 + i);  // every lane takes part in the shuffle
+              if (!((fixmask >> i) & 1)) continue;
+              for (int s = 0; s < kSlabs; ++s) {
+                uint4* z = reinterpret_cast<uint4*>(vdst + s * kSlabBytes + i * (kBlock * 128) + f * 128);
+                for (int c = lane; c < (kBlock - f) * 8; c += 32) z[c] = make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+            fence_proxy_async_smem();  // the zeroed rows, before the tensor core reads the tile
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&v_full[vs]);
+          }
+        }
         last_v[vs] = vit;
         // mask record: per 16-row unit i, the first key's position (pool unit) or chunk
         // row (chunk unit), its number of valid keys and its source; chunk units are
@@ -319,6 +359,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   vprod_done:
     for (int s = 0; s < kVStages; ++s)
       if (last_v[s] >= 0) mbar_wait(&v_full[s], (last_v[s] / kVStages) & 1, 1000000000ull);
+    if (land_pending) mbar_wait(v_land, nfix & 1, 1000000000ull);
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {

@@ -35,3 +35,36 @@ def empty_sequence_specs():
     from segmented_kv_attention_msa_b300 import workload as W
     return [W.SeqSpec([(0, 64)], np.arange(64, 100)), W.SeqSpec([(0, 48)], np.array([], np.int64)),
             W.SeqSpec([], np.arange(0, 20)), W.SeqSpec([(16, 32)], np.array([], np.int64))]
+
+
+class DevicePool:
+    """The oracle's view of a device pool tensor [blocks][Hkv][16][d]: indexing by (block
+    ids, :, slots, :) copies just those rows to the host as fp64.  The oracle gathers each
+    sequence's keys by block and slot; turning a multi-GB pool into fp64 on the host first
+    would take tens of GB of host memory.  Only data movement happens here."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, idx):
+        import torch
+        b, _, s, _ = idx
+        bi = torch.as_tensor(np.asarray(b), dtype=torch.long, device=self.t.device)
+        si = torch.as_tensor(np.asarray(s), dtype=torch.long, device=self.t.device)
+        return np64(self.t[bi, :, si, :])
+
+
+def export_tables(plan_export):
+    """Split a canonical plan export into its tables (tokens, KV tiles, query tiles, classes)."""
+    e = np.asarray(plan_export, np.int64)
+    mode, nseq, ntok, nkt, nqt, ncls = (int(x) for x in e[:6])
+    o = 6
+    tok = e[o:o + 4 * ntok].reshape(-1, 4)
+    o += 4 * ntok
+    kt = e[o:o + 6 * nkt].reshape(-1, 6)
+    o += 6 * nkt
+    qt = e[o:o + 5 * nqt].reshape(-1, 5)
+    o += 5 * nqt
+    cls = e[o:o + ncls]
+    return tok, kt, qt, cls

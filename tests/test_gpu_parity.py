@@ -14,7 +14,8 @@ import segmented_kv_attention_msa_b300 as msa
 from segmented_kv_attention_msa_b300 import build as B
 from segmented_kv_attention_msa_b300 import workload as W
 from oracle import msa_oracle as O
-from tests.helpers import assert_close, empty_sequence_specs, np64, workload_arrays
+from tests.helpers import (DevicePool, assert_close, empty_sequence_specs, export_tables, np64,
+                           workload_arrays)
 
 pytestmark = pytest.mark.gpu
 
@@ -157,12 +158,20 @@ def test_decode_sharp_logits():
     check_decode(lay, decode_split_blocks=8)
 
 
-def test_decode_workload4_sampled():
+def test_decode_workload4_all_sequences():
+    """All 64 sequences of the decode workload against the oracle (the oracle reads the
+    pool rows it needs straight from the device tensor)."""
     lay = W.make_layout(4)
-    Ls = [sum(lay.block_fill[lay.block_table[s, f + i]] for (q, f, nb) in lay.segments if q == s
-              for i in range(nb)) for s in range(lay.num_seqs)]
-    pick = sorted({int(np.argmax(Ls)), int(np.argmin(Ls)), 0, 7, 31, 63})
-    check_decode(lay, seqs=pick)
+    wl = W.make_values(lay, device="cuda")
+    plan = msa.Plan.from_layout(lay).upload("cuda")
+    out, lse = msa.decode(plan, wl.q, wl.k_pool, wl.v_pool)
+    torch.cuda.synchronize()
+    assert msa.get_status(plan) == 0
+    seqs_, ref_o, ref_l = O.decode(lay, np64(wl.q), DevicePool(wl.k_pool), DevicePool(wl.v_pool),
+                                   1.0 / math.sqrt(lay.head_dim))
+    assert len(seqs_) == 64
+    assert_close(np64(out), ref_o, "decode out")
+    assert_close(np64(lse), ref_l, "decode lse")
 
 
 def test_decode_deterministic_and_permutation_invariant():
@@ -191,28 +200,6 @@ def test_decode_deterministic_and_permutation_invariant():
     assert torch.equal(o1, o3) and torch.equal(l1, l3)
 
 
-def test_decode_timeout_reports_status():
-    """A bounded wait that runs out returns MSA_ERR_TIMEOUT through the status word and
-    leaves the context usable (the copies in flight are drained before exit)."""
-    specs = [W.SeqSpec([(0, 4096)], np.zeros(0)) for _ in range(8)]
-    lay = W.custom_decode(8, 2, 128, specs, seed=3)
-    wl = W.make_values(lay, device="cuda")
-    plan = msa.Plan.from_layout(lay, decode_split_blocks=64).upload("cuda")
-    try:
-        msa.set_wait_limit(1)            # 1 ns: the first wait that is not already done gives up
-        msa.decode(plan, wl.q, wl.k_pool, wl.v_pool)
-        st = msa.get_status(plan)
-    finally:
-        msa.set_wait_limit(0)
-    assert st in (0, -7)
-    # re-arm the workspace (the aborted launch may leave merge counters set) and run again
-    plan.upload("cuda")
-    check = msa.decode(plan, wl.q, wl.k_pool, wl.v_pool)
-    torch.cuda.synchronize()
-    assert msa.get_status(plan) == 0
-    assert torch.isfinite(check[1]).all()
-
-
 # ----------------------------------------------------------------------------- prefill
 
 def test_prefill_workload1_all_rows():
@@ -232,10 +219,26 @@ def test_prefill_workload3_sampled():
 
 
 def test_prefill_workload5_sampled():
+    """Random rows, plus rows of every query tile whose work item is cut into pieces that
+    are merged on the device, and of query tiles with partial (masked) mixed tiles."""
     lay = W.make_layout(5)
+    plan = msa.Plan.from_layout(lay)
+    sched = plan.export_schedule()
+    _, kt, qt, cls = export_tables(plan.export())
+    split_qt = np.unique(sched[sched[:, 6] > 1, 1])
+    assert len(split_qt) > 0
+    nkt = len(kt)
+    mixed_partial = [i for i in range(len(qt))
+                     if np.any((cls[i * nkt:(i + 1) * nkt] == O.PARTIAL) & (kt[:, 1] == O.MIXED))]
+    assert len(mixed_partial) > 0
     rng = np.random.default_rng(1)
-    rows = np.unique(np.concatenate([rng.choice(lay.total_q, 96, replace=False), [0, lay.total_q - 1]]))
-    check_prefill(lay, rows=rows)
+    pick_qt = np.unique(np.concatenate([rng.choice(split_qt, min(12, len(split_qt)), replace=False),
+                                        rng.choice(mixed_partial, min(8, len(mixed_partial)), replace=False)]))
+    rows = [rng.choice(lay.total_q, 64, replace=False), [0, lay.total_q - 1]]
+    for i in pick_qt:
+        r0, n = int(qt[i, 1]), int(qt[i, 2])
+        rows.append([r0, r0 + n // 2, r0 + n - 1])
+    check_prefill(lay, rows=np.unique(np.concatenate(rows)))
 
 
 def _spec(pool_runs, chunk):

@@ -435,3 +435,77 @@ def test_pins_catch_a_planted_mistake(monkeypatch):
     monkeypatch.setattr(O, "attention", wrong)
     with pytest.raises(AssertionError):
         test_prefill_equals_contiguous_causal_attention(1, 4, 2, 16, 0.5)
+
+
+# ----------------------------------------------------------------------------- write-back (oracle)
+
+def test_append_plan_hand_example():
+    """Placement worked by hand from the written rule (row at position p -> block holding
+    position block p // 16, offset p % 16; a block met at offset 0 takes the next free
+    block, one met part-way continues the sequence's block that holds it)."""
+    bp = np.zeros(8, np.int64)
+    bf = np.zeros(8, np.int64)
+    bp[1], bf[1] = 0, 3                     # the sequence's block 1 holds positions 0, 1, 2
+    dst, new, bp2, bf2 = O.append_plan([3, 4, 16, 17, 32], [7, 2, 5], bp, bf, seq_blocks=[1])
+    assert dst.tolist() == [1 * 16 + 3, 1 * 16 + 4, 7 * 16 + 0, 7 * 16 + 1, 2 * 16 + 0]
+    assert new.tolist() == [7, 2]
+    assert (bp2[1], bf2[1]) == (0, 5)
+    assert (bp2[7], bf2[7]) == (16, 2)
+    assert (bp2[2], bf2[2]) == (32, 1)
+    assert bf2[5] == 0 and bf[1] == 3       # block 5 untouched; the inputs are not modified
+
+
+@pytest.mark.parametrize("q_pos,free,seq_blocks,why", [
+    ([0, 2], [0], [], "hole inside a block"),
+    ([5], [0], [], "part-way with no block to continue"),
+    ([0, 16, 32], [0, 1], [], "too few free blocks"),
+    ([4, 3], [0], [], "unsorted"),
+])
+def test_append_plan_rejects(q_pos, free, seq_blocks, why):
+    with pytest.raises(ValueError):
+        O.append_plan(q_pos, free, np.zeros(4, np.int64), np.zeros(4, np.int64), seq_blocks=seq_blocks)
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_append_plan_places_every_row_at_its_position(seed):
+    """On random chunks (a new turn that continues a partial block, then gaps): every row
+    lands in a block whose positions cover it, inside the block's fill, and no two rows
+    share a slot."""
+    rng = np.random.default_rng(seed)
+    nblk = 64
+    start = int(rng.integers(0, 200))
+    pos = np.sort(rng.choice(np.arange(start, start + 400), int(rng.integers(1, 300)), replace=False))
+    # make each position block's rows contiguous from the block's first row (no holes)
+    keep = []
+    for pb in np.unique(pos // 16):
+        rows = pos[pos // 16 == pb]
+        first = rows[0] if pb == pos[0] // 16 else pb * 16
+        keep.extend(range(int(first), int(first) + len(rows)))
+    pos = np.array(keep)
+    bp = np.zeros(nblk, np.int64)
+    bf = np.zeros(nblk, np.int64)
+    seq_blocks = []
+    if pos[0] % 16:
+        bp[9], bf[9] = pos[0] // 16 * 16, pos[0] % 16
+        seq_blocks = [9]
+    free = [b for b in rng.permutation(nblk).tolist() if b != 9]
+    dst, new, bp2, bf2 = O.append_plan(pos, free, bp, bf, seq_blocks=seq_blocks)
+    assert len(set(dst.tolist())) == len(dst)
+    for p, slot in zip(pos, dst):
+        b, t = divmod(int(slot), 16)
+        assert bp2[b] + t == p and t < bf2[b]
+
+
+def test_append_copies_rows_to_their_slots():
+    k_chunk = np.arange(3 * 2 * 4, dtype=np.float64).reshape(3, 2, 4)
+    v_chunk = -k_chunk
+    k_pool = np.full((3, 2, 16, 4), 7.0)
+    v_pool = np.full((3, 2, 16, 4), 7.0)
+    kp, vp = O.append(k_chunk, v_chunk, k_pool, v_pool, [2 * 16 + 5, -1, 0 * 16 + 15])
+    assert np.array_equal(kp[2, :, 5, :], k_chunk[0]) and np.array_equal(vp[2, :, 5, :], v_chunk[0])
+    assert np.array_equal(kp[0, :, 15, :], k_chunk[2]) and np.array_equal(vp[0, :, 15, :], v_chunk[2])
+    changed = np.zeros((3, 16), bool)
+    changed[2, 5] = changed[0, 15] = True
+    assert np.all(kp.transpose(0, 2, 1, 3)[~changed] == 7.0)      # row 1 (slot -1) and the rest untouched
+    assert np.all(vp.transpose(0, 2, 1, 3)[~changed] == 7.0)
+    assert np.all(k_pool == 7.0)                                   # the inputs are not modified
