@@ -104,11 +104,15 @@ struct KTileHost {
 // consecutive stretches of near-equal cost; an item that straddles a cut becomes several
 // pieces, each computing a partial (O, max, sum) over its part of the list, merged on the
 // device by the piece that finishes last (log-sum-exp merge).  The cost model counts a
-// full tile as kWFull, a partial (masked) tile as kWPartial and each piece's set-up and
-// epilogue as kWPiece; no piece is shorter than kMinPiece tiles.  The smallest stretch
-// cost for which the walk fits in `ctas` CTAs is found by bisection.
+// full tile as kWFull, a partial (masked) tile as kWPartial, each piece's set-up and
+// epilogue as kWPiece, and each piece of a split item kWSplit more (its partial store, the
+// hand-shake, and the merge that one of them does).  The weights are B300 measurements:
+// per-CTA times of whole launches fitted by least squares to the CTAs' tile and piece
+// counts (a full tile ~1.9 us of a CTA's time, a masked tile 1.34 times that, a piece 2.8
+// full tiles, a split piece 5 more).  No piece is shorter than kMinPiece tiles.  The
+// smallest stretch cost for which the walk fits in `ctas` CTAs is found by bisection.
 constexpr int32_t kDefaultCtas = 148;
-constexpr int64_t kWFull = 8, kWPartial = 10, kWPiece = 8;
+constexpr int64_t kWFull = 8, kWPartial = 11, kWPiece = 22, kWSplit = 40;
 constexpr int32_t kMinPiece = 4;
 
 struct ItemRef {
@@ -139,16 +143,17 @@ bool walk_items(const std::vector<std::vector<int64_t>>& pre, const std::vector<
     }
     int32_t j = 0;
     while (j < n) {
-      const int64_t rest = w[n] - w[j] + kWPiece;
+      // the rest of the item as one piece: a split piece if an earlier piece took its start
+      const int64_t rest = w[n] - w[j] + kWPiece + (j > 0 ? kWSplit : 0);
       if (rest <= cap) {
         if (cuts) cuts->push_back({it, j, n - j, c});
         cap -= rest;
         j = n;
         break;
       }
-      // longest prefix of the rest that fits in what is left of this CTA
+      // longest prefix of the rest that fits in what is left of this CTA (a split piece)
       int32_t j2 = j;
-      while (j2 < n && w[j2 + 1] - w[j] + kWPiece <= cap) ++j2;
+      while (j2 < n && w[j2 + 1] - w[j] + kWPiece + kWSplit <= cap) ++j2;
       if (n - j2 < kMinPiece) j2 = n - kMinPiece;
       if (j2 - j >= kMinPiece) {
         if (cuts) cuts->push_back({it, j, j2 - j, c});

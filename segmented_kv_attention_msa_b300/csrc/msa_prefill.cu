@@ -123,6 +123,14 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   return d;
 }
 
+// One query row's D accumulator columns from TMEM: all loads issued, then one wait.
+template <int D>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&v)[D]) {
+#pragma unroll
+  for (int c = 0; c < D; c += 32) tmem_ld_x32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(&v[c]));
+  tmem_wait_ld();
+}
+
 // A KV tile record spread over a warp: lane i holds word i of the 32-word record.
 // Fields are read with warp shuffles, so every lane must take part.
 struct TileRec {
@@ -633,48 +641,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (releaser && lane == 0 && wq == 0) mbar_arrive(&v_empty[(it - 1) % kVStages]);  // last tile's V
       tc_fence_after();
       if (wk.nparts == 1) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const size_t orow = ((size_t)(qt.row0 + r) * p.Hq + h) * D;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tmem_ld_x32(tO + c, ov);
-          tmem_wait_ld();
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + orow + c);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
-              dst[q4] = v;
-            }
-          }
-        }
-        if (valid) p.lse[(size_t)(qt.row0 + r) * p.Hq + h] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+        // O leaves TMEM first, every column in flight at once, and the O columns are handed
+        // back before the rows are normalised and stored: the MMA warp may start the next
+        // piece's P.V meanwhile
+        uint32_t ov[D];
+        tmem_ld_row<D>(tO, ov);
         tc_fence_before();
         mbar_arrive(&o_free[t]);
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(qt.row0 + r) * p.Hq + h) * D);
+#pragma unroll
+          for (int q4 = 0; q4 < D / 8; ++q4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
+            dst[q4] = v;
+          }
+          p.lse[(size_t)(qt.row0 + r) * p.Hq + h] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+        }
       } else {
         // one piece of a split work item: store the unnormalised partial (O, max, sum);
         // the piece that finishes last merges all of them in slot order (log-sum-exp
         // merge), so the result does not depend on which piece that is.
         const size_t sb = (size_t)wk.slot * p.hpc + t;
         float4* po = p.part_o + sb * (D / 4) * 128;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tmem_ld_x32(tO + c, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            po[(size_t)(c / 4 + i) * 128 + r] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
-                                                            __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
-        }
-        p.part_ml[sb * 128 + r] = make_float2(m_used, l);
+        uint32_t ov[D];
+        tmem_ld_row<D>(tO, ov);
         tc_fence_before();
         mbar_arrive(&o_free[t]);
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i)
+          po[(size_t)i * 128 + r] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                                                __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+        p.part_ml[sb * 128 + r] = make_float2(m_used, l);
         // publish the partial device-wide, then one thread bumps the item's counter; the
         // handshake inside the CTA uses bounded mbarrier waits
         __threadfence();
@@ -688,41 +690,53 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!pf_wait_warp(&ep_flag[t], se & 1, p, abort_flag)) goto softmax_done;
         ++se;
         if (last_flag[t]) {
+          // The merge reads the parts from L2: every load of one part's half row is issued
+          // before any is used, so each part costs one round trip, not one per column.
           __threadfence();
           const size_t s0 = (size_t)wk.slot0 * p.hpc + t;
           float mx = -INFINITY;
+#pragma unroll 4
           for (int k = 0; k < wk.nparts; ++k) mx = fmaxf(mx, __ldcg(p.part_ml + (s0 + (size_t)k * p.hpc) * 128 + r).x);
-          float den = 0.f;
-          for (int k = 0; k < wk.nparts; ++k) {
-            const float2 ml = __ldcg(p.part_ml + (s0 + (size_t)k * p.hpc) * 128 + r);
-            den += (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - mx) * ml.y;
-          }
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          if (valid) {
-            const size_t orow = ((size_t)(qt.row0 + r) * p.Hq + h) * D;
+          float den = 0.f, inv = 0.f;
+          const size_t orow = ((size_t)(qt.row0 + r) * p.Hq + h) * D;
 #pragma unroll 1
-            for (int c4 = 0; c4 < D / 4; c4 += 2) {
-              float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-              for (int k = 0; k < wk.nparts; ++k) {
-                const size_t sk = s0 + (size_t)k * p.hpc;
-                const float mk = __ldcg(p.part_ml + sk * 128 + r).x;
-                const float wgt = (mk == -INFINITY) ? 0.f : fast_exp2(mk - mx);
-                const float4* pk = p.part_o + sk * (D / 4) * 128;
-                const float4 x0 = __ldcg(pk + (size_t)c4 * 128 + r), x1 = __ldcg(pk + (size_t)(c4 + 1) * 128 + r);
-                a0.x = fmaf(wgt, x0.x, a0.x); a0.y = fmaf(wgt, x0.y, a0.y);
-                a0.z = fmaf(wgt, x0.z, a0.z); a0.w = fmaf(wgt, x0.w, a0.w);
-                a1.x = fmaf(wgt, x1.x, a1.x); a1.y = fmaf(wgt, x1.y, a1.y);
-                a1.z = fmaf(wgt, x1.z, a1.z); a1.w = fmaf(wgt, x1.w, a1.w);
+          for (int half = 0; half < 2; ++half) {
+            float4 acc[D / 8];
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+            for (int k = 0; k < wk.nparts; ++k) {
+              const size_t sk = s0 + (size_t)k * p.hpc;
+              const float2 ml = __ldcg(p.part_ml + sk * 128 + r);
+              const float4* pk = p.part_o + (sk * (D / 4) + (size_t)half * (D / 8)) * 128 + r;
+              float4 x[D / 8];
+#pragma unroll
+              for (int i = 0; i < D / 8; ++i) x[i] = __ldcg(pk + (size_t)i * 128);
+              const float wgt = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - mx);
+              if (half == 0) den += wgt * ml.y;
+#pragma unroll
+              for (int i = 0; i < D / 8; ++i) {
+                acc[i].x = fmaf(wgt, x[i].x, acc[i].x);
+                acc[i].y = fmaf(wgt, x[i].y, acc[i].y);
+                acc[i].z = fmaf(wgt, x[i].z, acc[i].z);
+                acc[i].w = fmaf(wgt, x[i].w, acc[i].w);
               }
-              uint4 v;
-              v.x = pack_bf16x2(a0.x * inv, a0.y * inv);
-              v.y = pack_bf16x2(a0.z * inv, a0.w * inv);
-              v.z = pack_bf16x2(a1.x * inv, a1.y * inv);
-              v.w = pack_bf16x2(a1.z * inv, a1.w * inv);
-              *reinterpret_cast<uint4*>(p.out + orow + c4 * 4) = v;
             }
-            p.lse[(size_t)(qt.row0 + r) * p.Hq + h] = den > 0.f ? (mx + __log2f(den)) * kLn2 : -INFINITY;
+            if (half == 0) inv = den > 0.f ? 1.f / den : 0.f;
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + orow + half * (D / 2));
+#pragma unroll
+              for (int i = 0; i < D / 8; i += 2) {
+                uint4 v;
+                v.x = pack_bf16x2(acc[i].x * inv, acc[i].y * inv);
+                v.y = pack_bf16x2(acc[i].z * inv, acc[i].w * inv);
+                v.z = pack_bf16x2(acc[i + 1].x * inv, acc[i + 1].y * inv);
+                v.w = pack_bf16x2(acc[i + 1].z * inv, acc[i + 1].w * inv);
+                dst[i / 2] = v;
+              }
+            }
           }
+          if (valid) p.lse[(size_t)(qt.row0 + r) * p.Hq + h] = den > 0.f ? (mx + __log2f(den)) * kLn2 : -INFINITY;
           if (r == 0) *counter = 0;  // re-arm for the next launch
         }
       }
