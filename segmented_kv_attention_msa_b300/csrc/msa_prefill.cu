@@ -25,8 +25,8 @@
 //    works on S_0, the tensor core runs the other head's GEMMs.
 //  * warps 0-3 / 4-7 (softmax groups, one per head): each thread owns one query row in
 //    TMEM (tcgen05.ld 32x32b), masks partial tiles by a per-unit prefix cut, takes the
-//    exponentials against the running reference max while finding the tile max in the
-//    same pass (re-doing the pass only if the max grew by more than 2^8), writes P as
+//    exponentials against the running reference max (re-doing the pass against the
+//    tile's exact max only if the tile's sum of exponentials passes 2^16), writes P as
 //    bf16 back to TMEM, and at the end normalises O and stores bf16 rows and the LSE.
 //  * KV tiles whose smallest position exceeds the query tile's largest are never
 //    loaded (the planner leaves them out of the work item's list); tiles that every
@@ -557,11 +557,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               if (u >= cut) s[16 * b + u] = __float_as_uint(-INFINITY);
           }
         }
-        // Exponents are taken against the reference max m_used of the earlier tiles
-        // while this tile's max is found in the same pass (the two chains interleave).
-        // Only if the tile's max exceeds the reference by more than 2^8 is the pass
-        // redone against the new max, with O and l rescaled.  The first tile of a piece
-        // (reference still -inf) finds its max first.
+        // Exponents are taken against the reference max m_used of the earlier tiles.  The
+        // result is exact for any reference (O and l share it); the reference only has to
+        // keep the exponentials far from overflow.  So no max is tracked per element: only
+        // if the tile's sum of exponentials exceeds 2^16 (some exponential above 2^16, or
+        // not finite) is the tile's exact max found and the pass redone against it, with
+        // O and l rescaled.  The first tile of a piece (reference still -inf) finds its
+        // max first.
         float factor = 1.f;
         bool resc = false;
         const bool spec = !__any_sync(0xffffffffu, m_used == -INFINITY);
@@ -600,18 +602,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
               acc[c & 3] = fadd2(acc[c & 3], pe);
               pk[c] = pack_bf16x2(pe.x, pe.y);
-              if (c & 1)
-                m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], fmax3(__uint_as_float(s[e - 2]), __uint_as_float(s[e - 1]),
-                                                                 __uint_as_float(s[e])),
-                                         __uint_as_float(s[e + 1]));
             }
             tmem_st_x16(tS + q * 16, pk);
           }
           if (pass == 1 || !spec) break;
-          const float m_cand = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * p.scale_log2;
-          const bool redo = m_cand > m_used + 8.f;
+          // the tile's sum of exponentials bounds its largest one: above 2^16 (or not
+          // finite) the tile is redone against its exact max
+          const float2 at = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+          const bool redo = !(at.x + at.y <= 65536.f);
           if (!__any_sync(0xffffffffu, redo)) break;
           if (redo) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m4[i] = fmax3(__uint_as_float(s[i]), __uint_as_float(s[4 + i]), -INFINITY);
+#pragma unroll
+            for (int c = 8; c < 128; c += 8)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                m4[i] = fmax3(m4[i], __uint_as_float(s[c + i]), __uint_as_float(s[c + 4 + i]));
+            const float m_cand = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * p.scale_log2;
             factor = fast_exp2(m_used - m_cand);
             l *= factor;
             m_used = m_cand;

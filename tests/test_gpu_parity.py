@@ -365,17 +365,17 @@ def test_prefill_deterministic_and_permutation_invariant():
     assert torch.equal(o1, o3) and torch.equal(l1, l3)
 
 
-@pytest.mark.parametrize("ctas", [1, 2, 5, 37, 148, 1000])
+@pytest.mark.parametrize("ctas", [1, 2, 5, 8, 24, 37, 64, 148, 1000])
 def test_prefill_schedules(ctas):
     """The same layout balanced over different CTA counts: whole items, items cut into
-    2 or more pieces merged on the device; every schedule matches the oracle and is
-    bit-reproducible."""
+    2 or more pieces merged on the device (8, 24 and 64 CTAs and up cut some); every
+    schedule matches the oracle and is bit-reproducible."""
     rng = np.random.default_rng(31)
     specs = [W.random_prefill_spec(rng, 90, 0.5, 120, 900), W.random_prefill_spec(rng, 30, 0.3, 40, 300)]
     lay = W.custom_prefill(8, 2, 128, specs, seed=31, qk_std=0.5)
     plan = msa.Plan.from_layout(lay, prefill_ctas=ctas)
     sc = plan.export_schedule()
-    if ctas >= 37:
+    if ctas in (8, 24) or ctas >= 64:
         assert (sc[:, 6] > 1).any()          # some items are split and merged
     wl, o1, l1 = check_prefill(lay, plan_kw={"prefill_ctas": ctas})
     _, o2, l2 = run_prefill(lay, wl, {"prefill_ctas": ctas})
