@@ -756,6 +756,110 @@ def run_sweep(args):
     print(json.dumps(res), flush=True)
 
 
+# ----------------------------------------------------------------------------- eviction policy
+
+# Eq. 5 coefficients of the two-segment latency model fitted to this kernel's timings on
+# B300 (bench.py --sweep; ms per 16-token block): k5 and k2 - k3 + k5
+EVICT_K5 = 3.07463e-6
+EVICT_KCONST = 1.10065e-4 - 7.83825e-5 + 3.07463e-6
+
+
+def modelled_recompute_cost(hit, k5=EVICT_K5, k_const=EVICT_KCONST):
+    """Modelled recompute time of one request (ms): Eq. 5's marginal cost
+    k5 (l1 + 2 q1) + (k2 - k3 + k5) summed over its recomputed blocks in position order,
+    l1 and q1 the cached and recomputed blocks before each."""
+    cost, l1, q1 = 0.0, 0, 0
+    for h in hit:
+        if h:
+            l1 += 1
+        else:
+            cost += k5 * (l1 + 2 * q1) + k_const
+            q1 += 1
+    return cost
+
+
+def replay_trace(policy, trace, capacity, k5=EVICT_K5, k_const=EVICT_KCONST):
+    """Serve a request trace (time, session, context blocks) through a cache of
+    `capacity` blocks managed by `policy` (insert / access / victim).  A request reads
+    blocks 0 .. n-1 of its session: cached ones are hits (accessed), the rest are
+    recomputed and cached; then the policy evicts until the cache fits again (any block,
+    this request's included: its KV has been used).  Returns hit counts and the modelled
+    recompute time, with and without the cache."""
+    cached = set()
+    hits = total = 0
+    cost = cost_none = 0.0
+    for (now, sess, n) in trace:
+        ids = [sess * 65536 + b for b in range(n)]
+        hit = [b in cached for b in ids]
+        for b, h in zip(ids, hit):
+            if h:
+                policy.access(b, now)
+        for pb, (b, h) in enumerate(zip(ids, hit)):
+            if not h:
+                policy.insert(b, pb, now)
+                cached.add(b)
+        while len(cached) > capacity:
+            cached.remove(policy.victim(now))
+        hits += sum(hit)
+        total += n
+        cost += modelled_recompute_cost(hit, k5, k_const)
+        cost_none += modelled_recompute_cost([False] * n, k5, k_const)
+    return {"hits": hits, "blocks": total, "hit_rate": hits / max(1, total), "modelled_ms": cost,
+            "modelled_ms_no_cache": cost_none}
+
+
+def run_evict(args):
+    """Eviction policies on a synthetic multi-turn trace (prints its own JSON line): the
+    cost-aware policy against LRU and prefix-only at several cache sizes (hit rate and
+    modelled recompute time), and the time per eviction of the O(log n) structure against
+    the O(n) scan and LRU at 4k-10k cached blocks (the comparison of Fig. 8)."""
+    import numpy as np
+    import segmented_kv_attention_msa_b300 as msa
+    from segmented_kv_attention_msa_b300 import build as B
+    from segmented_kv_attention_msa_b300 import workload as W
+    if not os.path.exists(msa.LIB_PATH):
+        B.build()
+    trace = W.multiturn_trace()
+    final = {}
+    for (_, s, n) in trace:
+        final[s] = n
+    distinct = sum(final.values())
+    res = {"kind": "eviction_policy_synthetic_trace", "trace": {"requests": len(trace), "sessions": len(final),
+           "distinct_blocks": distinct, "blocks_read": sum(n for _, _, n in trace), "generator": "workload.multiturn_trace()"},
+           "model": {"k5": EVICT_K5, "k_const": EVICT_KCONST, "unit": "ms per 16-token block"},
+           "policies": {}}
+    for frac in (0.1, 0.2, 0.4):
+        cap = int(distinct * frac)
+        row = {}
+        for name in ("lru", "prefix", "cost"):
+            t0 = time.perf_counter()
+            r = replay_trace(msa.EvictionPolicy(name), trace, cap)
+            r["wall_s"] = round(time.perf_counter() - t0, 2)
+            r["hit_rate"] = round(r["hit_rate"], 4)
+            r["modelled_ms"] = round(r["modelled_ms"], 1)
+            r["modelled_ms_no_cache"] = round(r["modelled_ms_no_cache"], 1)
+            row[name] = r
+        res["policies"][f"capacity_{int(frac * 100)}pct"] = {"capacity_blocks": cap, **row}
+    # time per eviction at n cached blocks: insert n, then alternate evict / insert
+    timing = {}
+    rng = np.random.default_rng(5)
+    for n in (4000, 6000, 8000, 10000):
+        row = {}
+        for name in ("lru", "cost", "cost_scan"):
+            p = msa.EvictionPolicy(name, period=0)
+            for b in range(n):
+                p.insert(b, int(rng.integers(0, 4096)), float(b % 97))
+            reps = 2000
+            t0 = time.perf_counter()
+            for k in range(reps):
+                p.victim(100.0 + k)
+                p.insert(n + k, int(rng.integers(0, 4096)), 100.0 + k)
+            row[name] = round((time.perf_counter() - t0) / reps * 1e6, 2)
+        timing[str(n)] = row
+    res["us_per_evict_and_insert"] = timing
+    print(json.dumps(res), flush=True)
+
+
 def _single_kernel_result(args, world, pl, dl, pst, dst, pf_mean, dc_mean, peaks, peak_kind, clocks):
     """Result line of a one-kernel run (--only), used for profiling captures."""
     res = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "only": args.only,
@@ -895,11 +999,16 @@ def main(argv=None):
     ap.add_argument("--no-ablation", action="store_true", help="skip the per-segment launch comparison")
     ap.add_argument("--sweep", action="store_true",
                     help="cached-ratio sweep and latency-model fit (prints its own JSON line, not the bench line)")
+    ap.add_argument("--evict", action="store_true",
+                    help="eviction policies on a synthetic multi-turn trace (prints its own JSON line; no GPU)")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="time one kernel alone (for profiling captures); not the bench line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.evict:
+        run_evict(args)
+        return
     world, rank, local = dist_setup()
     if args.sweep:
         if rank == 0:

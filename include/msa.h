@@ -295,6 +295,62 @@ void msa_set_wait_limit(int64_t ns);
  * default). */
 void msa_set_test_drop(int32_t kernel, int32_t cta, int32_t index);
 
+/* ------------------------------------------------------------------ eviction policy
+ * Host-side KV-block eviction policy (abstract: eviction that jointly weighs hit rate and
+ * position-aware recompute cost; Fig. 6 / Eq. 5: the marginal recompute latency of a
+ * block; Fig. 7 / Fig. 8: reuse-time distribution and a piecewise exponential reuse model
+ * in an O(log n) structure; Fig. 10 / Eq. 10: the lambda update from the mean block
+ * lifespan; appendix A.1: only an exponential keeps the order of blocks not accessed).
+ * No GPU is involved.  Score of a cached block b at time t, the smallest evicted first:
+ *   S_b(t) = C_b * min(1, lambda * F_b * exp(-(t - t_b) / beta)),
+ *   C_b = k5 * p_b + k_const   (Eq. 5 with l1 + 2 q1 approximated by p_b, the number of
+ *                               blocks before b in its sequence; k_const = k2 - k3 + k5),
+ *   F_b = accesses of b while cached, t_b = its last access,
+ *   lambda = exp((tau - tau0) / beta - tau / alpha)   (Eq. 10), tau = the mean lifespan
+ *   (eviction time - insertion time) of the last `window` evicted blocks, refreshed every
+ *   `period` evictions (period 0: lambda stays lambda0).
+ * Ties go to the smaller block id.  Times are any increasing unit (e.g. request count). */
+typedef enum {
+  MSA_EVICT_COST = 0,       /* the score above, ordered sets: O(log n) per operation */
+  MSA_EVICT_COST_SCAN = 1,  /* the same score by a linear scan per eviction: O(n) */
+  MSA_EVICT_LRU = 2,        /* baseline: least recently accessed first */
+  MSA_EVICT_PREFIX = 3      /* baseline, prefix caching: largest position first (then LRU) */
+} msa_evict_policy_t;
+
+typedef struct {
+  double k5;         /* Eq. 5 coefficient of (l1 + 2 q1), per block, > = 0 */
+  double k_const;    /* k2 - k3 + k5, > 0 (so every C_b > 0) */
+  double beta;       /* time scale of the exponential (and of Eq. 10), > 0 */
+  double alpha;      /* Eq. 10, > 0 */
+  double tau0;       /* Eq. 10 */
+  double lambda0;    /* lambda before the first update, > 0 */
+  int32_t window;    /* lifespans in the sliding window (> 0 when period > 0) */
+  int32_t period;    /* evictions between lambda updates, 0 = never */
+  int32_t policy;    /* msa_evict_policy_t */
+  int32_t reserved;  /* must be 0 */
+} msa_evict_opts_t;
+
+typedef struct msa_evict msa_evict_t;  /* opaque, host-owned */
+
+/* Errors: INVALID_ARG (a bad option, an unknown or duplicate block, an empty cache on
+ * victim, a non-finite time).  Block ids are any non-negative int32. */
+msa_status_t msa_evict_create(const msa_evict_opts_t* opts, msa_evict_t** out);
+void msa_evict_destroy(msa_evict_t* policy);
+/* A block enters the cache (its first access) at time `now`; pos_block = p_b. */
+msa_status_t msa_evict_insert(msa_evict_t* policy, int32_t block, int32_t pos_block, double now);
+/* A cached block is accessed again (a hit). */
+msa_status_t msa_evict_access(msa_evict_t* policy, int32_t block, double now);
+/* A block leaves the cache without being evicted (e.g. its sequence ended). */
+msa_status_t msa_evict_remove(msa_evict_t* policy, int32_t block);
+/* Choose the block to evict at time `now`, remove it and record its lifespan. */
+msa_status_t msa_evict_victim(msa_evict_t* policy, double now, int32_t* block);
+/* S_b(now) of a cached block (cost-aware definition, whatever the policy). */
+msa_status_t msa_evict_score(const msa_evict_t* policy, int32_t block, double now, double* score);
+msa_status_t msa_evict_get_lambda(const msa_evict_t* policy, double* lambda);
+int32_t msa_evict_size(const msa_evict_t* policy);
+/* Consistency check of the policy's internal ordered sets (for tests). */
+msa_status_t msa_evict_check(const msa_evict_t* policy, double now);
+
 const char* msa_status_string(msa_status_t status);
 int32_t msa_version(void);
 

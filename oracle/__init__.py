@@ -5,3 +5,5 @@ import this package.  It shares no code with the CUDA path.
 """
 from .msa_oracle import (attention, canonical_plan, canonical_tokens, chunk_sizes, decode,  # noqa: F401
                          gather_by_position, merge_lse, prefill, seq_units, useful_flops)
+from .evict_oracle import (EvictOracle, lambda_update, marginal_cost, modelled_recompute_cost,  # noqa: F401
+                           recompute_cost, reuse_estimate, turning_point)

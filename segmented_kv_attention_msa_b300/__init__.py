@@ -48,6 +48,13 @@ class _Stats(ctypes.Structure):
                 ("num_split_items", ctypes.c_int32)]
 
 
+class _EvictOpts(ctypes.Structure):
+    _fields_ = [("k5", ctypes.c_double), ("k_const", ctypes.c_double), ("beta", ctypes.c_double),
+                ("alpha", ctypes.c_double), ("tau0", ctypes.c_double), ("lambda0", ctypes.c_double),
+                ("window", ctypes.c_int32), ("period", ctypes.c_int32), ("policy", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 _lib = None
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -79,6 +86,16 @@ EXPORTS = {
     "msa_get_status": (_I32, [_P, _P]),
     "msa_set_wait_limit": (None, [ctypes.c_int64]),
     "msa_set_test_drop": (None, [_I32, _I32, _I32]),
+    "msa_evict_create": (_I32, [ctypes.POINTER(_EvictOpts), ctypes.POINTER(_P)]),
+    "msa_evict_destroy": (None, [_P]),
+    "msa_evict_insert": (_I32, [_P, _I32, _I32, ctypes.c_double]),
+    "msa_evict_access": (_I32, [_P, _I32, ctypes.c_double]),
+    "msa_evict_remove": (_I32, [_P, _I32]),
+    "msa_evict_victim": (_I32, [_P, ctypes.c_double, _I32P]),
+    "msa_evict_score": (_I32, [_P, _I32, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]),
+    "msa_evict_get_lambda": (_I32, [_P, ctypes.POINTER(ctypes.c_double)]),
+    "msa_evict_size": (_I32, [_P]),
+    "msa_evict_check": (_I32, [_P, ctypes.c_double]),
     "msa_status_string": (ctypes.c_char_p, [_I32]),
     "msa_version": (_I32, []),
 }
@@ -427,3 +444,59 @@ def set_test_drop(kernel: str = None, cta: int = -1, index: int = -1):
     leave out one copy so that the wait for it runs out.  No argument turns it off."""
     k = {"prefill": 0, "decode": 1}.get(kernel, -1)
     lib().msa_set_test_drop(k, int(cta), int(index))
+
+
+
+EVICT_POLICIES = {"cost": 0, "cost_scan": 1, "lru": 2, "prefix": 3}
+
+
+class EvictionPolicy:
+    """Host-side KV-block eviction policy of the library (msa_evict_* in include/msa.h):
+    the cost-aware score (Eq. 5 recompute cost times a piecewise exponential reuse
+    estimate, lambda from Eq. 10), or the LRU / prefix-only baselines."""
+
+    def __init__(self, policy: str = "cost", k5: float = 3.07463e-6, k_const: float = 3.49e-5,
+                 beta: float = 16.0, alpha: float = 64.0, tau0: float = 0.0, lambda0: float = 1.0,
+                 window: int = 64, period: int = 16):
+        opts = _EvictOpts(k5, k_const, beta, alpha, tau0, lambda0, window, period, EVICT_POLICIES[policy], 0)
+        h = ctypes.c_void_p(0)
+        _check(lib().msa_evict_create(ctypes.byref(opts), ctypes.byref(h)), "msa_evict_create")
+        self._h = h
+        self.policy = policy
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.msa_evict_destroy(h)
+            self._h = None
+
+    def insert(self, block: int, pos_block: int, now: float):
+        _check(lib().msa_evict_insert(self._h, int(block), int(pos_block), float(now)), "msa_evict_insert")
+
+    def access(self, block: int, now: float):
+        _check(lib().msa_evict_access(self._h, int(block), float(now)), "msa_evict_access")
+
+    def remove(self, block: int):
+        _check(lib().msa_evict_remove(self._h, int(block)), "msa_evict_remove")
+
+    def victim(self, now: float) -> int:
+        b = ctypes.c_int32(-1)
+        _check(lib().msa_evict_victim(self._h, float(now), ctypes.byref(b)), "msa_evict_victim")
+        return int(b.value)
+
+    def score(self, block: int, now: float) -> float:
+        v = ctypes.c_double(0.0)
+        _check(lib().msa_evict_score(self._h, int(block), float(now), ctypes.byref(v)), "msa_evict_score")
+        return float(v.value)
+
+    @property
+    def lam(self) -> float:
+        v = ctypes.c_double(0.0)
+        _check(lib().msa_evict_get_lambda(self._h, ctypes.byref(v)), "msa_evict_get_lambda")
+        return float(v.value)
+
+    def __len__(self) -> int:
+        return int(lib().msa_evict_size(self._h))
+
+    def check(self, now: float = 0.0) -> bool:
+        return lib().msa_evict_check(self._h, float(now)) == 0

@@ -440,3 +440,29 @@ def random_prefill_spec(rng: np.random.Generator, old_blocks: int, cached_frac: 
     sizes = [R - c, c] if R > c else [R]
     runs_pool, cpos = _split_recompute(~cached, old_blocks * BLOCK_SIZE, suffix, sizes)
     return SeqSpec(_cached_runs_tokens(cached) + runs_pool, cpos)
+
+
+# ----------------------------------------------------------------------------- request traces
+
+def multiturn_trace(seed: int = 20260100, sessions: int = 64, requests: int = 4000,
+                    first_blocks=(16, 256), turn_blocks=(1, 16), popularity_sigma: float = 1.0):
+    """A synthetic multi-session, multi-turn request trace (the paper's LooGLE / BFCL
+    traces are not available).  Each session starts with a context of U[first_blocks]
+    blocks; each of its turns adds U[turn_blocks] blocks and reads the whole context.  At
+    every time step one session makes a request, picked with a fixed lognormal popularity
+    weight, so reuse times are spread (popular sessions return soon, others rarely).
+    Returns a list of (time, session, context blocks)."""
+    rng = np.random.default_rng(seed)
+    weights = rng.lognormal(0.0, popularity_sigma, sessions)
+    weights /= weights.sum()
+    length = rng.integers(first_blocks[0], first_blocks[1] + 1, sessions)
+    grow = rng.integers(turn_blocks[0], turn_blocks[1] + 1, sessions)
+    started = np.zeros(sessions, bool)
+    trace = []
+    for t in range(requests):
+        s = int(rng.choice(sessions, p=weights))
+        if started[s]:
+            length[s] += grow[s]
+        started[s] = True
+        trace.append((t, s, int(length[s])))
+    return trace
