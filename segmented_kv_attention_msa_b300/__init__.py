@@ -18,7 +18,8 @@ from typing import Optional, Sequence
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmsa.so")
+# MSA_LIBRARY=debug selects the MSA_DEBUG build (device-side bounds checks; build.py --debug)
+LIB_PATH = os.path.join(_PKG, "libmsa_debug.so" if os.environ.get("MSA_LIBRARY") == "debug" else "libmsa.so")
 
 MSA_PREFILL, MSA_DECODE = 0, 1
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "position overlap",

@@ -105,6 +105,11 @@ extern "C" msa_status_t msa_prefill(const msa_plan_t* plan, const void* plan_dev
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = g_wait_ns.load();
   test_drop(0, &p.drop_cta, &p.drop_k);
+  p.n_qt = plan->n_qt;
+  p.n_kt = plan->n_kt;
+  p.n_list = plan->n_list;
+  p.total_q = plan->total_q;
+  p.num_pool_blocks = plan->num_pool_blocks;
   PrefillTensors T{q, k_chunk, v_chunk, k_pool, v_pool, plan->total_q, pool_blocks, plan->d};
   return launch_prefill(p, T, stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
@@ -141,6 +146,9 @@ extern "C" msa_status_t msa_decode(const msa_plan_t* plan, const void* plan_dev,
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = g_wait_ns.load();
   test_drop(1, &p.drop_split, &p.drop_k);
+  p.n_blist = plan->n_blist;
+  p.num_pool_blocks = plan->num_pool_blocks;
+  p.num_seqs = plan->num_seqs;
   return launch_decode(p, plan->d, plan->n_split, stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

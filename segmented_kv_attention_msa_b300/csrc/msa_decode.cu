@@ -88,6 +88,14 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const SplitRec sp = p.split[blockIdx.x];
+#ifdef MSA_DEBUG
+  // the split must point inside the plan's block list, sequences and splits
+  if (!MSA_DCHECK(sp.blk_begin >= 0 && sp.blk_count >= 0 && sp.blk_begin + sp.blk_count <= p.n_blist &&
+                      sp.seq >= 0 && sp.seq < p.num_seqs && sp.first_split >= 0 && sp.nsplit >= 1 &&
+                      sp.first_split + sp.nsplit <= (int)gridDim.x,
+                  p.status))
+    return;
+#endif
   const int groups = p.G / GH;
   const int g = blockIdx.y / groups;
   const int h0 = g * p.G + (blockIdx.y % groups) * GH;
@@ -127,7 +135,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
     const int phys = p.blist[bi];
     const int st = k % kDecStages;
     uint8_t* dst = ring + st * S::kStageBytes;
-    const int y = (phys * p.Hkv + g) * kBlock;
+    // (a block id outside the pool reads rows past it, which arrive as zeros)
+    const int y = MSA_DCHECK(phys >= 0 && phys < p.num_pool_blocks, p.status) ? (phys * p.Hkv + g) * kBlock
+                                                                                : (int)p.pool_rows;
     mbar_arrive_expect_tx(&full_bar[warp][st], S::kStageBytes);
 #pragma unroll
     for (int s = 0; s < S::kSlabs; ++s) tma_load_2d(dst + s * S::kSlabBytes, &tm_k, &full_bar[warp][st], s * 64, y);
@@ -156,7 +166,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
   for (; k < nb_w; ++k) {
     const int st = k % kDecStages;
     const int bi = sp.blk_begin + warp + kDecWarps * k;
-    const int fill = p.bfill[bi];
+    int fill = p.bfill[bi];
+    if (!MSA_DCHECK(fill >= 1 && fill <= kBlock, p.status)) fill = fill < 1 ? 0 : kBlock;
     if (!mbar_wait(&full_bar[warp][st], (k / kDecStages) & 1, p.wait_ns)) {
       set_status(p.status, MSA_ERR_TIMEOUT);
       aborted = true;

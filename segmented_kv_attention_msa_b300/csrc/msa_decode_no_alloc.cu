@@ -94,6 +94,9 @@ extern "C" msa_status_t msa_decode_no_alloc(const msa_plan_t* plan, const void* 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_ns = wait_limit_ns();  // the same bound as every other launch (msa_set_wait_limit)
   test_drop(1, &p.drop_split, &p.drop_k);
+  p.n_blist = plan->n_blist;
+  p.num_pool_blocks = plan->num_pool_blocks;
+  p.num_seqs = plan->num_seqs;
   return launch_decode(p, plan->d, plan->n_split, stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

@@ -208,4 +208,13 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Bounds checks of the MSA_DEBUG build: a record that points outside the plan or the
+// pool sets MSA_ERR_BLOCK_OOB and is replaced by a safe value (no trap).  In the regular
+// build the condition is not evaluated.
+#ifdef MSA_DEBUG
+#define MSA_DCHECK(ok, status) ((ok) ? true : (set_status((status), MSA_ERR_BLOCK_OOB), false))
+#else
+#define MSA_DCHECK(ok, status) true
+#endif
+
 }  // namespace msa

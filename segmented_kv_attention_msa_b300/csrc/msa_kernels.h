@@ -25,6 +25,7 @@ struct PrefillParams {
   float scale_log2;
   uint64_t wait_ns;
   int32_t drop_cta, drop_k;  // test hook: CTA drop_cta leaves out its K tile number drop_k (-1: none)
+  int32_t n_qt, n_kt, n_list, total_q, num_pool_blocks;  // bounds checked by the MSA_DEBUG build
 };
 
 struct PrefillTensors {
@@ -51,6 +52,7 @@ struct DecodeParams {
   float scale_log2;
   uint64_t wait_ns;
   int32_t drop_split, drop_k;  // test hook: warp 0 of CTA (drop_split, 0) leaves out its block drop_k (-1: none)
+  int32_t n_blist, num_pool_blocks, num_seqs;  // bounds checked by the MSA_DEBUG build
 };
 
 struct GatherParams {

@@ -139,8 +139,29 @@ struct TileRec {
 };
 __device__ __forceinline__ TileRec load_tile_rec(const PrefillParams& p, const int* lst, int j, int lane) {
   const int e = __ldg(lst + j);
-  const int* rec = reinterpret_cast<const int*>(p.kt + (e & 0x7fffffff));
+  int ki = e & 0x7fffffff;
+  if (!MSA_DCHECK(ki < p.n_kt, p.status)) ki = 0;
+  const int* rec = reinterpret_cast<const int*>(p.kt + ki);
   return TileRec{__ldg(rec + lane)};
+}
+
+// MSA_DEBUG build: a work record must point inside the plan (query tile, list range, heads)
+// before any role reads through it; a bad one sets MSA_ERR_BLOCK_OOB and the CTA gives up.
+__device__ __forceinline__ bool work_ok(const PrefillParams& p, const WorkRec& wk) {
+#ifdef MSA_DEBUG
+  bool ok = wk.qt >= 0 && wk.qt < p.n_qt && wk.g >= 0 && wk.g < p.Hkv && wk.h0 >= 0 && wk.h0 + p.hpc <= p.Hq &&
+            wk.j0 >= 0 && wk.n >= 0 && p.hpc >= 1 && p.hpc <= 2;
+  if (ok) {
+    const QTileRec qt = p.qt[wk.qt];
+    ok = qt.list_begin >= 0 && qt.list_begin + wk.j0 + wk.n <= p.n_list && qt.row0 >= 0 && qt.nrows >= 0 &&
+         qt.row0 + qt.nrows <= p.total_q;
+  }
+  return MSA_DCHECK(ok, p.status);
+#else
+  (void)p;
+  (void)wk;
+  return true;
+#endif
 }
 
 // Issue the TMA loads of one K or V tile (whole warp calls; lane 0 posts the byte
@@ -150,7 +171,7 @@ __device__ __forceinline__ TileRec load_tile_rec(const PrefillParams& p, const i
 template <int D>
 __device__ __forceinline__ void issue_kv_tile(const TileRec& rec, uint8_t* dst, uint64_t* bar,
                                               const CUtensorMap* tm_chunk, const CUtensorMap* tm_pool,
-                                              int g, int Hkv, int pool_rows, int lane) {
+                                              int g, const PrefillParams& p, int lane) {
   constexpr int kSlabs = D / 64;
   const int nblk = rec.get(3);
   const int blk = rec.get(8 + (lane & 7));
@@ -158,10 +179,15 @@ __device__ __forceinline__ void issue_kv_tile(const TileRec& rec, uint8_t* dst, 
   __syncwarp();
   if (lane < kTileBlocks) {
     uint8_t* d = dst + lane * 2048;
-    if (lane < nblk && blk < 0) {
+    bool chunk = false;
+    int y = p.pool_rows;  // past the pool: the box arrives as zeros
+    if (lane < nblk && MSA_DCHECK(blk < 0 ? -blk - 1 < p.total_q : blk < p.num_pool_blocks, p.status)) {
+      chunk = blk < 0;
+      if (!chunk) y = (blk * p.Hkv + g) * kBlock;
+    }
+    if (chunk) {
       for (int s = 0; s < kSlabs; ++s) tma_load_2d(d + s * kSlabBytes, tm_chunk, bar, g * D + s * 64, -blk - 1);
     } else {
-      const int y = (lane < nblk) ? (blk * Hkv + g) * kBlock : pool_rows;
       for (int s = 0; s < kSlabs; ++s) tma_load_2d(d + s * kSlabBytes, tm_pool, bar, s * 64, y);
     }
   }
@@ -254,6 +280,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     int last_wi = -1;
     for (int w = cta_w0; w < cta_w1; ++w) {
       const WorkRec wk = p.work[w];
+      if (!work_ok(p, wk)) {
+        *abort_flag = 1;
+        goto kprod_done;
+      }
       const QTileRec qt = p.qt[wk.qt];
       const int n = wk.n;
       if (n == 0) continue;
@@ -274,8 +304,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!pf_wait_warp(&k_empty[ks], ((kit / kKStages) & 1) ^ 1, p, abort_flag)) goto kprod_done;
         // (test hook: one CTA may leave out one K tile, so that the wait for it runs out)
         if (!(kit == p.drop_k && (int)blockIdx.x == p.drop_cta)) {
-          issue_kv_tile<D>(cur, sK + ks * L::kTileBytes, &k_full[ks], &tm_kc, &tm_kp, wk.g, p.Hkv, p.pool_rows,
-                           lane);
+          issue_kv_tile<D>(cur, sK + ks * L::kTileBytes, &k_full[ks], &tm_kc, &tm_kp, wk.g, p, lane);
           last_k[ks] = kit;
         }
         ++kit;
@@ -296,6 +325,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     bool land_pending = false;  // a copy on v_land has not been seen to land
     for (int w = cta_w0; w < cta_w1; ++w) {
       const WorkRec wk = p.work[w];
+      if (!work_ok(p, wk)) {
+        *abort_flag = 1;
+        goto vprod_done;
+      }
       const QTileRec qt = p.qt[wk.qt];
       const int n = wk.n;
       if (n == 0) continue;
@@ -319,9 +352,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const bool fix_u = lane < kTileBlocks && ui < u_n && u_blk >= 0 && u_fill < kBlock;
           const unsigned fixmask = __ballot_sync(0xffffffffu, fix_u);
           if (fixmask == 0) {
-            issue_kv_tile<D>(cur, vdst, &v_full[vs], &tm_vc, &tm_vp, wk.g, p.Hkv, p.pool_rows, lane);
+            issue_kv_tile<D>(cur, vdst, &v_full[vs], &tm_vc, &tm_vp, wk.g, p, lane);
           } else {
-            issue_kv_tile<D>(cur, vdst, v_land, &tm_vc, &tm_vp, wk.g, p.Hkv, p.pool_rows, lane);
+            issue_kv_tile<D>(cur, vdst, v_land, &tm_vc, &tm_vp, wk.g, p, lane);
             land_pending = true;
             if (!pf_wait_warp(v_land, nfix & 1, p, abort_flag)) goto vprod_done;
             land_pending = false;
@@ -409,6 +442,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       auto mma_loop = [&](auto hpc_c) {
         constexpr int HPC = decltype(hpc_c)::value;
         for (int w = cta_w0; w < cta_w1; ++w) {
+          if (!work_ok(p, p.work[w])) {
+            *abort_flag = 1;
+            return;
+          }
           const int n = p.work[w].n;
           if (n == 0) continue;
           if (!pf_wait(q_full, wi & 1, p, abort_flag)) return;
@@ -494,6 +531,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     int it = 0, wi = 0, se = 0;  // tiles, pieces and split pieces done
     for (int w = cta_w0; w < cta_w1; ++w) {
       const WorkRec wk = p.work[w];
+      if (!work_ok(p, wk)) {
+        *abort_flag = 1;
+        goto softmax_done;
+      }
       const QTileRec qt = p.qt[wk.qt];
       const int n = wk.n;
       if (n == 0) {
