@@ -166,29 +166,12 @@ bool walk_items(const std::vector<std::vector<int64_t>>& pre, const std::vector<
   return true;
 }
 
-void schedule_prefill(const std::vector<QTileRec>& qts, const std::vector<int32_t>& list,
-                      const std::vector<ItemRef>& items, int32_t ctas, std::vector<WorkRec>& work,
-                      std::vector<int32_t>& cta_begin, std::vector<int32_t>& sched) {
-  work.clear();
-  cta_begin.assign(1, 0);
-  sched.clear();
-  if (items.empty()) return;
-  std::vector<std::vector<int64_t>> pre(items.size());
+// Cut one list of items (in `order`) into stretches over `ctas` CTAs, the smallest
+// stretch cost that fits found by bisection; CTA indices run backwards when `reverse`.
+void balance(const std::vector<std::vector<int64_t>>& pre, const std::vector<int32_t>& order, int32_t ctas,
+             bool reverse, std::vector<Cut>& cuts) {
   int64_t total = 0;
-  for (size_t i = 0; i < items.size(); ++i) {
-    const QTileRec& q = qts[items[i].qt];
-    std::vector<int64_t>& w = pre[i];
-    w.assign(q.list_count + 1, 0);
-    for (int32_t j = 0; j < q.list_count; ++j)
-      w[j + 1] = w[j] + (list[q.list_begin + j] < 0 ? kWPartial : kWFull);
-    total += w.back() + kWPiece;
-  }
-  // longest first; ties keep (query tile, KV head, head) order
-  std::vector<int32_t> order(items.size());
-  std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int32_t a, int32_t b) { return pre[a].back() > pre[b].back(); });
-  ctas = std::max<int32_t>(1, ctas);
+  for (int32_t it : order) total += pre[it].back() + kWPiece;
   // with T = total everything fits in one CTA, so the bisection always ends feasible
   int64_t lo = (total + ctas - 1) / ctas, hi = total;
   while (lo < hi) {
@@ -196,36 +179,84 @@ void schedule_prefill(const std::vector<QTileRec>& qts, const std::vector<int32_
     if (walk_items(pre, order, mid, ctas, nullptr)) hi = mid;
     else lo = mid + 1;
   }
-  std::vector<Cut> cuts;
   walk_items(pre, order, lo, ctas, &cuts);
-  // pieces per item, partial slots for items in several pieces
-  std::vector<int32_t> nparts(items.size(), 0), slot0(items.size(), -1), seen(items.size(), 0);
-  for (const Cut& c : cuts) ++nparts[c.item];
+  if (reverse)
+    for (Cut& c : cuts) c.cta = ctas - 1 - c.cta;
+}
+
+// KV-head phases.  Every work item streams the KV tiles of its KV head.  When the KV of all
+// heads together is larger than the L2 cache can hold, CTAs that run items of different
+// heads at the same time evict each other's tiles, and every item re-reads its tiles from
+// DRAM.  So then the items are balanced head by head and every CTA runs its share of head
+// 0, then of head 1, and so on: at any time the CTAs read one head's KV (the walk runs
+// forwards for even heads and backwards for odd ones, so that the remainders of the
+// per-head balancing land on different CTAs).
+constexpr int64_t kPhaseKvBytes = 96ll << 20;
+
+void schedule_prefill(const std::vector<QTileRec>& qts, const std::vector<int32_t>& list,
+                      const std::vector<ItemRef>& items, int32_t ctas, int32_t Hkv, int64_t kv_bytes,
+                      std::vector<WorkRec>& work, std::vector<int32_t>& cta_begin, std::vector<int32_t>& sched) {
+  work.clear();
+  cta_begin.assign(1, 0);
+  sched.clear();
+  if (items.empty()) return;
+  std::vector<std::vector<int64_t>> pre(items.size());
+  for (size_t i = 0; i < items.size(); ++i) {
+    const QTileRec& q = qts[items[i].qt];
+    std::vector<int64_t>& w = pre[i];
+    w.assign(q.list_count + 1, 0);
+    for (int32_t j = 0; j < q.list_count; ++j)
+      w[j + 1] = w[j] + (list[q.list_begin + j] < 0 ? kWPartial : kWFull);
+  }
+  ctas = std::max<int32_t>(1, ctas);
+  const bool phased = kv_bytes > kPhaseKvBytes && Hkv > 1;
+  const int32_t nphase = phased ? Hkv : 1;
+  // longest first within each phase; ties keep (query tile, KV head, head) order
+  std::vector<std::vector<Cut>> cuts(nphase);
+  for (int32_t ph = 0; ph < nphase; ++ph) {
+    std::vector<int32_t> order;
+    for (int32_t i = 0; i < (int32_t)items.size(); ++i)
+      if (!phased || items[i].g == ph) order.push_back(i);
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int32_t a, int32_t b) { return pre[a].back() > pre[b].back(); });
+    balance(pre, order, ctas, phased && (ph & 1), cuts[ph]);
+  }
+  // pieces per item (numbered in list order, the walk's order), partial slots for items
+  // in several pieces
+  std::vector<int32_t> nparts(items.size(), 0), slot0(items.size(), -1);
+  std::vector<std::vector<int32_t>> part(nphase);
+  for (int32_t ph = 0; ph < nphase; ++ph)
+    for (const Cut& c : cuts[ph]) part[ph].push_back(nparts[c.item]++);
   int32_t slots = 0;
-  for (int32_t it : order)
-    if (nparts[it] > 1) {
-      slot0[it] = slots;
-      slots += nparts[it];
-    }
-  const int32_t used = cuts.empty() ? 0 : cuts.back().cta + 1;
-  // within a CTA, pieces of split items run first (their merges then happen early),
-  // then whole items, each group in walk order
-  for (int32_t c = 0, k = 0; c < used; ++c) {
-    int32_t k1 = k;
-    while (k1 < (int32_t)cuts.size() && cuts[k1].cta == c) ++k1;
-    for (int pass = 0; pass < 2; ++pass)
-      for (int32_t i = k; i < k1; ++i) {
-        const Cut& cu = cuts[i];
-        const bool split = nparts[cu.item] > 1;
-        if ((pass == 0) != split) continue;
-        const ItemRef& r = items[cu.item];
-        const int32_t slot = split ? slot0[cu.item] + seen[cu.item]++ : -1;
-        work.push_back({r.qt, r.g, r.h0, cu.j0, cu.n, nparts[cu.item], slot0[cu.item], slot});
-        const int32_t rec[9] = {c, r.qt, r.g, r.h0, cu.j0, cu.n, nparts[cu.item], slot0[cu.item], slot};
-        sched.insert(sched.end(), rec, rec + 9);
+  for (const std::vector<Cut>& cs : cuts)
+    for (const Cut& c : cs)
+      if (nparts[c.item] > 1 && slot0[c.item] < 0) {
+        slot0[c.item] = slots;
+        slots += nparts[c.item];
       }
+  // each CTA runs its pieces phase by phase; within a phase, pieces of split items first
+  // (their merges then happen early), then whole items, each group in walk order
+  std::vector<std::vector<std::vector<int32_t>>> by_cta(ctas, std::vector<std::vector<int32_t>>(nphase));
+  for (int32_t ph = 0; ph < nphase; ++ph)
+    for (int32_t i = 0; i < (int32_t)cuts[ph].size(); ++i) by_cta[cuts[ph][i].cta][ph].push_back(i);
+  int32_t used = 0;
+  for (int32_t c = 0; c < ctas; ++c)
+    for (int32_t ph = 0; ph < nphase; ++ph)
+      if (!by_cta[c][ph].empty()) used = c + 1;
+  for (int32_t c = 0; c < used; ++c) {
+    for (int32_t ph = 0; ph < nphase; ++ph)
+      for (int pass = 0; pass < 2; ++pass)
+        for (int32_t i : by_cta[c][ph]) {
+          const Cut& cu = cuts[ph][i];
+          const bool split = nparts[cu.item] > 1;
+          if ((pass == 0) != split) continue;
+          const ItemRef& r = items[cu.item];
+          const int32_t slot = split ? slot0[cu.item] + part[ph][i] : -1;
+          work.push_back({r.qt, r.g, r.h0, cu.j0, cu.n, nparts[cu.item], slot0[cu.item], slot});
+          const int32_t rec[9] = {c, r.qt, r.g, r.h0, cu.j0, cu.n, nparts[cu.item], slot0[cu.item], slot};
+          sched.insert(sched.end(), rec, rec + 9);
+        }
     cta_begin.push_back((int32_t)work.size());
-    k = k1;
   }
 }
 
@@ -458,7 +489,8 @@ extern "C" msa_status_t msa_plan_create(const msa_plan_opts_t* opts, msa_mode_t 
         for (int32_t h = 0; h < P->G; h += P->hpc) items.push_back({(int32_t)qi, g, g * P->G + h});
     }
     const int32_t ctas = opts->prefill_ctas > 0 ? opts->prefill_ctas : kDefaultCtas;
-    schedule_prefill(qts, list, items, ctas, work, cta_begin, sched);
+    const int64_t kv_bytes = (int64_t)P->n_tok * Hkv * P->d * 2 * 2;  // K and V, bf16
+    schedule_prefill(qts, list, items, ctas, Hkv, kv_bytes, work, cta_begin, sched);
     P->n_ctas = (int32_t)cta_begin.size() - 1;
     P->n_slots = 0;
     for (const WorkRec& w : work)
