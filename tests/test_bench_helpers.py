@@ -50,15 +50,19 @@ def test_traffic_record_keyed_on_code_and_workload(tmp_path, monkeypatch):
     csrc = tmp_path / "segmented_kv_attention_msa_b300" / "csrc"
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
-    code = "__global__ void k() {}\n"
+    code, plan = "__global__ void k() {}\n", "int plan() { return 1; }\n"
     (csrc / "k.cu").write_text(code)
-    (tmp_path / "profiles" / "k_traffic.txt").write_text(
-        f"applies_to: wl_a\ncode_sha256: {bench.code_sha256(code)}\ndram_bytes_per_launch: 1234\n")
+    (csrc / "p.cpp").write_text(plan)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.kernel_traffic("k", "k.cu", "wl_a") == 1234.0
-    assert bench.kernel_traffic("k", "k.cu", "wl_b") is None              # another workload
+    monkeypatch.setitem(bench.TRAFFIC_SOURCES, "k", ("k.cu", "p.cpp"))
+    (tmp_path / "profiles" / "k_traffic.txt").write_text(
+        f"applies_to: wl_a\ncode_sha256: {bench.sources_sha256('k')}\ndram_bytes_per_launch: 1234\n")
+    assert bench.kernel_traffic("k", "wl_a") == 1234.0
+    assert bench.kernel_traffic("k", "wl_b") is None              # another workload
     (csrc / "k.cu").write_text("// a comment\n" + code)
-    assert bench.kernel_traffic("k", "k.cu", "wl_a") == 1234.0            # comment-only edit
+    assert bench.kernel_traffic("k", "wl_a") == 1234.0            # comment-only edit
+    (csrc / "p.cpp").write_text("int plan() { return 2; }\n")
+    assert bench.kernel_traffic("k", "wl_a") is None              # the planner changed
+    (csrc / "p.cpp").write_text(plan)
     (csrc / "k.cu").write_text("__global__ void k() { int x = 1; (void)x; }\n")
-    assert bench.kernel_traffic("k", "k.cu", "wl_a") is None              # the kernel changed
-
+    assert bench.kernel_traffic("k", "wl_a") is None              # the kernel changed
