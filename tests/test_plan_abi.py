@@ -430,3 +430,25 @@ def test_append_plan_errors():
     with pytest.raises(msa.MSAError):
         msa.append_plan([0, 1, 16, 18], [2, 5], b3, f3)
     assert not b3.any() and not f3.any()
+
+
+def test_prefill_schedule_kv_head_phases():
+    """When the KV of all heads is larger than L2 holds (the 131k-token context: 541 MB),
+    every CTA runs its pieces KV head by KV head, and each head's work is balanced over
+    the CTAs on its own; when it fits (the 8192-token context: 37 MB) the schedule is one
+    longest-first walk whose CTAs mix heads."""
+    big = W.make_layout(5)
+    sc = msa.Plan.from_layout(big).export_schedule()
+    for c in np.unique(sc[:, 0]):
+        g = sc[sc[:, 0] == c, 2]
+        assert np.all(np.diff(g) >= 0)                       # head 0 first, then head 1, ...
+    _, kt, qt, cls = export_tables(msa.Plan.from_layout(big).export())
+    per_head = np.zeros((148, big.num_heads_kv))
+    for c, q, g, h0, j0, n, nparts, s0, slot in sc:
+        per_head[c, g] += n
+    for g in range(big.num_heads_kv):
+        col = per_head[:, g]
+        assert col.max() <= 1.06 * np.median(col)            # each head balanced on its own
+    small = W.make_layout(2)
+    sc2 = msa.Plan.from_layout(small).export_schedule()
+    assert any(np.any(np.diff(sc2[sc2[:, 0] == c, 2]) < 0) for c in np.unique(sc2[:, 0]))
