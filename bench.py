@@ -975,7 +975,9 @@ def run_reference(args, world, rank):
     pw = W.make_values(pl, device="cpu")
     arrays = {k: getattr(pw, k).float().numpy().astype(np.float64)
               for k in ("q", "k_chunk", "v_chunk", "k_pool", "v_pool")}
-    rows = sample_rows(pl, args.ref_rows, 1e11)
+    # the whole run stays within a few minutes: about 2.5e12 useful FLOPs over all the timed
+    # steps (the oracle does ~0.03 TFLOP/s on 16 cores), at most 1e11 per step
+    rows = sample_rows(pl, args.ref_rows, min(1e11, 2.5e12 / max(1, args.steps)))
     for _ in range(args.warmup):
         oracle_prefill_sample(pl, arrays, rows[:8])
     t = [oracle_prefill_sample(pl, arrays, rows) for _ in range(args.steps)]
@@ -1011,7 +1013,8 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="query rows of the oracle baseline (0: as many as about 6e11 useful FLOPs)")
     ap.add_argument("--ref-rows", type=int, default=0,
-                    help="query rows per reference-arm step (0: as many as about 1e11 useful FLOPs)")
+                    help="query rows per reference-arm step (0: as many as about min(1e11, 2.5e12 / steps) "
+                         "useful FLOPs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true", help="skip the per-segment launch comparison")
     ap.add_argument("--sweep", action="store_true",
