@@ -17,7 +17,9 @@
 //    as zeros.
 //  * warp 11 (V producer): the V tiles into a 2-deep ring, and for each tile a mask
 //    record (per unit: its source, the position or chunk row of its first key and its
-//    number of valid keys) used by partial tiles.
+//    number of valid keys) used by partial tiles.  A pool block holding fewer than 16
+//    keys may carry anything (NaN included) in its unused slots: those V rows are zeroed
+//    in shared memory before the slot is marked full.
 //  * warp 8 (MMA issuer, one thread of it): tcgen05.mma kind::f16.  S_t = Q_t K^T (both
 //    operands in 128-byte-swizzled shared memory, accumulator in TMEM), then
 //    O_t += P_t V with P_t read from TMEM (it overwrites S_t as bf16) and V as an
