@@ -635,19 +635,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const float2 nms2 = make_float2(-ms, -ms);
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+          uint32_t pk[64];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               const int e = q * 32 + 2 * c;
               const float2 x = ffma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), scale2, nms2);
               const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
               acc[c & 3] = fadd2(acc[c & 3], pe);
-              pk[c] = pack_bf16x2(pe.x, pe.y);
+              pk[q * 16 + c] = pack_bf16x2(pe.x, pe.y);
             }
-            tmem_st_x16(tS + q * 16, pk);
           }
+          // P leaves in two x32 stores after the whole pass: measured faster than a store
+          // per 32 exponentials, which interleaves store issue with the exponential chain
+          tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
           if (pass == 1 || !spec) break;
           // the tile's sum of exponentials bounds its largest one: above 2^16 (or not
           // finite) the tile is redone against its exact max
