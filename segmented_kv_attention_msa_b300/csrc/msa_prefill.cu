@@ -20,11 +20,13 @@
 //    number of valid keys) used by partial tiles.  A pool block holding fewer than 16
 //    keys may carry anything (NaN included) in its unused slots: those V rows are zeroed
 //    in shared memory before the slot is marked full.
-//  * warp 8 (MMA issuer, one thread of it): tcgen05.mma kind::f16.  S_t = Q_t K^T (both
-//    operands in 128-byte-swizzled shared memory, accumulator in TMEM), then
-//    O_t += P_t V with P_t read from TMEM (it overwrites S_t as bf16) and V as an
-//    MN-major shared-memory operand.  The two heads ping-pong: while one softmax group
-//    works on S_0, the tensor core runs the other head's GEMMs.
+//  * warps 8 and 9 (MMA issuers, one thread each, warp 8 for head 0, warp 9 for head 1):
+//    tcgen05.mma kind::f16.  S_t = Q_t K^T (both operands in 128-byte-swizzled shared
+//    memory, accumulator in TMEM), then O_t += P_t V with P_t read from TMEM (it
+//    overwrites S_t as bf16) and V as an MN-major shared-memory operand.  The two heads
+//    ping-pong: while one softmax group works on S_0, the tensor core runs the other
+//    head's GEMMs.  The issuers pass a turn between them so that the heads' blocks
+//    alternate; each waits for its own head's P while the other issues.
 //  * warps 0-3 / 4-7 (softmax groups, one per head): each thread owns one query row in
 //    TMEM (tcgen05.ld 32x32b), masks partial tiles by a per-unit prefix cut, takes the
 //    exponentials against the running reference max (re-doing the pass against the
@@ -34,7 +36,7 @@
 //    loaded (the planner leaves them out of the work item's list); tiles that every
 //    query row sees fully skip the mask.
 //  * Registers: the softmax warpgroups hold a full 128-column row of S and run with 216
-//    registers a thread; the third warpgroup (MMA issuer, producers) gives its share
+//    registers a thread; the third warpgroup (MMA issuers, producers) gives its share
 //    back (setmaxnreg).
 // TMEM: 512 columns = S_0 | S_1 | O_0 | O_1 (128 columns each).
 #include <cuda.h>
@@ -48,7 +50,7 @@
 
 namespace msa {
 
-// 12 warps = 3 full warpgroups (setmaxnreg acts on whole warpgroups); warp 9 idles.
+// 12 warps = 3 full warpgroups (setmaxnreg acts on whole warpgroups).
 // At launch every thread gets kPfLaunchRegs registers (65536 / 384, rounded down to 8);
 // the split below must fit in that total, and the host refuses to launch a build whose
 // kernel was given fewer registers.
@@ -67,7 +69,7 @@ constexpr int kMaskInts = 24;          // mask record: base[8], nvalid[8], src[8
 template <int D>
 struct PfLayout {
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kNumBars = 29;
+  static constexpr int kNumBars = 31;
   static constexpr int kBar = 0;
   static constexpr int kMisc = (kBar + kNumBars * 8 + 15) / 16 * 16;  // TMEM base address, flags
   static constexpr int kMask = kMisc + 16;                             // int32 [kVStages][kMaskInts]
@@ -223,6 +225,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* ep_bar = bars + 24;    // [2] split pieces: the head's 128 threads stored their partial
   uint64_t* ep_flag = bars + 26;   // [2] split pieces: merge counter read, last_flag[t] valid
   uint64_t* v_land = bars + 28;    // V tiles with unused pool slots: the copy landed (then fixed up)
+  uint64_t* turn = bars + 29;      // [2] head t's issuer may start its next block
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + L::kMisc + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem_raw + L::kMisc + 8);  // [2]
@@ -238,14 +241,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    // Q, K and V slots are handed back once per head: each head's GEMMs come from
+    // their own issuing thread, and one head's completion says nothing of the other's
+    mbar_init(q_empty, p.hpc);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+      mbar_init(&k_empty[s], p.hpc);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_empty[s], p.hpc);
       mbar_init(&m_full[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -259,6 +264,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
     mbar_init(v_land, 1);
+    mbar_init(&turn[0], 1);
+    mbar_init(&turn[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -403,8 +410,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int s = 0; s < kVStages; ++s)
       if (last_v[s] >= 0) mbar_wait(&v_full[s], (last_v[s] / kVStages) & 1, 1000000000ull);
     if (land_pending) mbar_wait(v_land, nfix & 1, 1000000000ull);
-  } else if (warp == 8) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp - 8 < p.hpc) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 8 issues head 0's GEMMs, warp 9 head 1's.  One thread cannot issue a
+    // 128x128x16 MMA as fast as the tensor pipe retires it once a softmax warp shares
+    // its scheduler, and a head's next block waits on its own P only: with a thread per
+    // head, neither head's block queues behind the other's.
+    const int t = warp - 8;
     if (lane == 0) {
       // one descriptor per operand ring, built once.  Slot and k-step offsets add to the
       // start-address field in the low word (addresses stay below 2^18, so the field never
@@ -413,36 +425,45 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       constexpr uint32_t kTileDesc = (uint32_t)(L::kTileBytes >> 4);
       const uint64_t qd0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint32_t desc_hi = (uint32_t)(qd0 >> 32);
-      const uint32_t q_lo = (uint32_t)qd0;
+      const uint32_t q_lo = (uint32_t)qd0 + (uint32_t)t * kTileDesc;
       const uint32_t k_lo = (uint32_t)smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint32_t v_lo = (uint32_t)smem_desc_sw128(smem_u32(sV), kSlabBytes, 1024);
+      const uint32_t tS = tmem + t * 128, tO = tmem + 256 + t * 128;
       auto desc = [&](uint32_t lo) { return ((uint64_t)desc_hi << 32) | lo; };
       int it = 0, wi = 0, ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0;  // phase bits of the K and V rings at (ks, vs)
+      // The two heads' blocks take turns (0, 1, 0, 1, ...): left free, both issuers start
+      // together, their GEMMs share the pipe and their softmax groups the MUFU, and the
+      // two heads stay in step.  Block nb of head 1 follows block nb of head 0; block nb
+      // of head 0 follows block nb - 1 of head 1.
+      int nb = 0;
+      auto my_turn = [&]() {
+        if (p.hpc == 1 || (t == 0 && nb == 0)) return true;
+        return pf_wait(&turn[t], (uint32_t)((t == 0 ? nb - 1 : nb) & 1), p, abort_flag);
+      };
+      auto pass_turn = [&]() {
+        if (p.hpc == 2) mbar_arrive(&turn[1 - t]);
+        ++nb;
+      };
       // (the empty asm keeps the compiler from hoisting all 16 descriptors of a block out
       // of the loops: this warpgroup runs with 64 registers)
-      auto issue_qk = [&](int t, int kslot) {
-        uint32_t qd = q_lo + (uint32_t)t * kTileDesc, kd = k_lo + (uint32_t)kslot * kTileDesc;
+      auto issue_qk = [&](int kslot) {
+        uint32_t qd = q_lo, kd = k_lo + (uint32_t)kslot * kTileDesc;
         asm volatile("" : "+r"(qd), "+r"(kd));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (uint32_t)((((kk >> 2) * kSlabBytes) + (kk & 3) * 32) >> 4);
-          umma_ss(tmem + t * 128, desc(qd + off), desc(kd + off), kIdescQK, kk > 0);
+          umma_ss(tS, desc(qd + off), desc(kd + off), kIdescQK, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, int vslot, bool acc) {
+      auto issue_pv = [&](int vslot, bool acc) {
         uint32_t vd = v_lo + (uint32_t)vslot * kTileDesc;
         asm volatile("" : "+r"(vd));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc(vd + (uint32_t)((kk * 2048) >> 4)), kIdescPV,
-                  (acc || kk > 0) ? 1u : 0u);
+          umma_ts(tO, tS + kk * 8, desc(vd + (uint32_t)((kk * 2048) >> 4)), kIdescPV, (acc || kk > 0) ? 1u : 0u);
       };
-      // HPC (query heads per CTA) is a compile-time constant here so that the head loop
-      // unrolls: between two heads' GEMM blocks this thread does as little as possible,
-      // since it shares its scheduler with a busy softmax warp.
-      auto mma_loop = [&](auto hpc_c) {
-        constexpr int HPC = decltype(hpc_c)::value;
+      [&] {
         for (int w = cta_w0; w < cta_w1; ++w) {
           if (!work_ok(p, p.work[w])) {
             *abort_flag = 1;
@@ -452,64 +473,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (n == 0) continue;
           if (!pf_wait(q_full, wi & 1, p, abort_flag)) return;
           if (!pf_wait(&k_full[ks], kph, p, abort_flag)) return;
+          if (!my_turn()) return;
           tc_fence_after();
-#pragma unroll
-          for (int t = 0; t < HPC; ++t) {
-            issue_qk(t, ks);
-            umma_commit(&s_full[t]);
-          }
+          issue_qk(ks);
+          umma_commit(&s_full[t]);
+          pass_turn();
           if (n == 1) umma_commit(q_empty);
           if (++ks == kKStages) { ks = 0; kph ^= 1; }
-          bool v_ok = false, k_ok = false;  // V of tile j / K of tile j+1 already seen full
           for (int j = 0; j < n; ++j) {
-            const int cur = it + j;
             const bool has_next = j + 1 < n;
-            // ring slots (and phases) of the next tile's V and of the K after it
-            int vs2 = vs + 1, ks2 = ks + 1;
-            uint32_t vph2 = vph, kph2 = kph;
-            if (vs2 == kVStages) { vs2 = 0; vph2 ^= 1; }
-            if (ks2 == kKStages) { ks2 = 0; kph2 ^= 1; }
-#pragma unroll
-            for (int t = 0; t < HPC; ++t) {
-              if (!pf_wait(&p_full[t], cur & 1, p, abort_flag)) return;
-              if (t == 0) {
-                if (!v_ok && !pf_wait(&v_full[vs], vph, p, abort_flag)) return;
-                if (has_next && !k_ok && !pf_wait(&k_full[ks], kph, p, abort_flag)) return;
-              }
-              if (j == 0 && !pf_wait(&o_free[t], (wi & 1) ^ 1, p, abort_flag)) return;
-              tc_fence_after();
-              issue_pv(t, vs, j > 0);
-              if (t == HPC - 1) {
-                // while the pipe works through these products, look (without waiting)
-                // whether the next tile's V and the K after it have landed
-                v_ok = has_next && mbar_test_wait(&v_full[vs2], vph2);
-                k_ok = j + 2 < n && mbar_test_wait(&k_full[ks2], kph2);
-              }
-              if (has_next) {
-                issue_qk(t, ks);
-                umma_commit(&s_full[t]);
-              } else {
-                umma_commit(&o_full[t]);
-              }
+            if (!pf_wait(&p_full[t], (it + j) & 1, p, abort_flag)) return;
+            if (!pf_wait(&v_full[vs], vph, p, abort_flag)) return;
+            if (has_next && !pf_wait(&k_full[ks], kph, p, abort_flag)) return;
+            if (j == 0 && !pf_wait(&o_free[t], (wi & 1) ^ 1, p, abort_flag)) return;
+            if (!my_turn()) return;
+            tc_fence_after();
+            issue_pv(vs, j > 0);
+            if (has_next) {
+              issue_qk(ks);
+              umma_commit(&s_full[t]);
+              if (++ks == kKStages) { ks = 0; kph ^= 1; }
+            } else {
+              umma_commit(&o_full[t]);
             }
-            // the K and V slots are handed back by the last softmax group once it sees
+            pass_turn();
+            // this head's K and V slots are handed back by its softmax group once it sees
             // the S (or O) that these GEMMs produced: that commit covers every MMA above
-            if (has_next) { ks = ks2; kph = kph2; }
             if (j + 2 == n) umma_commit(q_empty);
-            vs = vs2;
-            vph = vph2;
+            if (++vs == kVStages) { vs = 0; vph ^= 1; }
           }
           it += n;
           ++wi;
         }
-      };
-      if (p.hpc == 2)
-        mma_loop(std::integral_constant<int, 2>{});
-      else
-        mma_loop(std::integral_constant<int, 1>{});
+      }();
       // every exit (done or aborted) waits for its MMAs in flight before TMEM is freed
-      umma_commit(&drain[0]);
-      mbar_wait(&drain[0], 0, 1000000000ull);
+      umma_commit(&drain[t]);
+      mbar_wait(&drain[t], 0, 1000000000ull);
     }
     __syncwarp();
   }
@@ -557,7 +556,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       const int h = wk.h0 + t;
       const bool valid = r < qt.nrows;
-      const bool releaser = t == p.hpc - 1;
       // rows past the tile's end see every key (their values are finite and never stored)
       const int qp = valid ? __ldg(p.qpos + qt.row0 + r) : 0x7fffffff;
       const int qrow = valid ? qt.row0 + r : 0x7fffffff;
@@ -569,9 +567,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const bool partial = e_next < 0;
         if (j + 1 < n) e_next = __ldg(lst + j + 1);
         if (!pf_wait_warp(&s_full[t], it & 1, p, abort_flag)) goto softmax_done;
-        if (releaser && lane == 0 && wq == 0) {
-          // S of this tile for the last head is done: every MMA issued before it is too,
-          // so this tile's K slot and the previous tile's V slot are free
+        if (lane == 0 && wq == 0) {
+          // S of this tile for this head is done, and so is every MMA its issuing thread
+          // started before it: for this head, this tile's K slot and the previous tile's
+          // V slot are free
           mbar_arrive(&k_empty[it % kKStages]);
           if (j > 0) mbar_arrive(&v_empty[(it - 1) % kVStages]);
         }
@@ -692,7 +691,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       // epilogue: O / l -> bf16, LSE = ln 2 * (m + log2 l)
       if (!pf_wait_warp(&o_full[t], wi & 1, p, abort_flag)) goto softmax_done;
-      if (releaser && lane == 0 && wq == 0) mbar_arrive(&v_empty[(it - 1) % kVStages]);  // last tile's V
+      if (lane == 0 && wq == 0) mbar_arrive(&v_empty[(it - 1) % kVStages]);  // last tile's V
       tc_fence_after();
       if (wk.nparts == 1) {
         // O leaves TMEM first, every column in flight at once, and the O columns are handed
