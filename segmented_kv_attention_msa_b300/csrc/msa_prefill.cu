@@ -304,6 +304,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int t = 0; t < p.hpc; ++t)
           for (int s = 0; s < kSlabs; ++s)
             tma_load_2d(sQ + t * L::kTileBytes + s * kSlabBytes, &tm_q, q_full, (wk.h0 + t) * D + s * 64, qt.row0);
+        // The next item's Q can load only once this item's last QK^T is done, and then
+        // waits behind the K/V tiles in flight: bring it into L2 now, while this item runs.
+        if (w + 1 < cta_w1) {
+          const WorkRec wn = p.work[w + 1];
+          if (wn.n > 0 && work_ok(p, wn)) {
+            const int row0n = p.qt[wn.qt].row0;
+            for (int t = 0; t < p.hpc; ++t)
+              for (int s = 0; s < kSlabs; ++s) tma_prefetch_2d(&tm_q, (wn.h0 + t) * D + s * 64, row0n);
+          }
+        }
       }
       last_wi = wi;
       for (int j = 0; j < n; ++j) {
@@ -703,15 +713,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         mbar_arrive(&o_free[t]);
         const float inv = l > 0.f ? 1.f / l : 0.f;
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(qt.row0 + r) * p.Hq + h) * D);
+          // 32-byte stores (rows start on 256-byte boundaries)
+          __nv_bfloat16* dst = p.out + ((size_t)(qt.row0 + r) * p.Hq + h) * D;
 #pragma unroll
-          for (int q4 = 0; q4 < D / 8; ++q4) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
-            dst[q4] = v;
+          for (int c = 0; c < D; c += 16) {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(ov[c + 2 * i]) * inv, __uint_as_float(ov[c + 2 * i + 1]) * inv);
+            st_global_v8(dst + c, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
           }
           p.lse[(size_t)(qt.row0 + r) * p.Hq + h] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
         }
@@ -777,16 +787,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             if (half == 0) inv = den > 0.f ? 1.f / den : 0.f;
             if (valid) {
-              uint4* dst = reinterpret_cast<uint4*>(p.out + orow + half * (D / 2));
+              __nv_bfloat16* dst = p.out + orow + half * (D / 2);
 #pragma unroll
-              for (int i = 0; i < D / 8; i += 2) {
-                uint4 v;
-                v.x = pack_bf16x2(acc[i].x * inv, acc[i].y * inv);
-                v.y = pack_bf16x2(acc[i].z * inv, acc[i].w * inv);
-                v.z = pack_bf16x2(acc[i + 1].x * inv, acc[i + 1].y * inv);
-                v.w = pack_bf16x2(acc[i + 1].z * inv, acc[i + 1].w * inv);
-                dst[i / 2] = v;
-              }
+              for (int i = 0; i < D / 8; i += 4)
+                st_global_v8(dst + i * 4, pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
+                             pack_bf16x2(acc[i].z * inv, acc[i].w * inv),
+                             pack_bf16x2(acc[i + 1].x * inv, acc[i + 1].y * inv),
+                             pack_bf16x2(acc[i + 1].z * inv, acc[i + 1].w * inv),
+                             pack_bf16x2(acc[i + 2].x * inv, acc[i + 2].y * inv),
+                             pack_bf16x2(acc[i + 2].z * inv, acc[i + 2].w * inv),
+                             pack_bf16x2(acc[i + 3].x * inv, acc[i + 3].y * inv),
+                             pack_bf16x2(acc[i + 3].z * inv, acc[i + 3].w * inv));
             }
           }
           if (valid) p.lse[(size_t)(qt.row0 + r) * p.Hq + h] = den > 0.f ? (mx + __log2f(den)) * kLn2 : -INFINITY;
