@@ -436,6 +436,8 @@ def run_ours(args, world, rank, local):
     e2e_pf, e2e_dc, ser_pf, ser_dc = reduce_max([e2e_pf, e2e_dc, ser_pf, ser_dc], world, dev)
 
     append = append_bench(msa, W, pl, pw, dev, flush)
+    merge = merge_bench(msa, pl, dev, flush, hbm_peak, peak_kind)
+    gather = gather_bench(msa, pplan, pw, dev, flush, hbm_peak, peak_kind)
     configs = {}
     for idx in PREFILL_WORKLOADS:
         if idx == args.workload:
@@ -502,6 +504,8 @@ def run_ours(args, world, rank, local):
                            "prefill_ms": round(ser_pf, 4), "decode_ms": round(ser_dc, 4)}},
         "prefill_configs": configs,
         "append": append,
+        "merge": merge,
+        "gather": gather,
         "ablation_per_segment": ablation,
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
@@ -587,6 +591,63 @@ def append_bench(msa, W, pl, pw, dev, flush, reps: int = 20):
     ms = statistics.median(ts)
     nbytes = 2 * 2 * n * pl.num_heads_kv * pl.head_dim * 2
     return {"rows": n, "bytes": nbytes, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+
+
+def _time_device(run, flush, reps: int = 20):
+    """Median CUDA-event time (ms) of run() after 3 warm-up calls, L2 flushed before each."""
+    import torch
+    for _ in range(3):
+        run()
+    ts = []
+    for _ in range(reps):
+        flush.fill_(5)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def merge_bench(msa, pl, dev, flush, hbm_peak, peak_kind):
+    """The stand-alone LSE merge (two fp32 partials -> bf16 O and fp32 LSE) at the prefill
+    output's shape; not part of the step.  Bytes = both partials and LSEs read, O and LSE
+    written."""
+    import torch
+    rows, heads, d = pl.total_q, pl.num_heads_q, pl.head_dim
+    g = torch.Generator(device=dev).manual_seed(20260117)
+    o_a = torch.randn(rows, heads, d, generator=g, device=dev)
+    o_b = torch.randn(rows, heads, d, generator=g, device=dev)
+    l_a = torch.randn(rows, heads, generator=g, device=dev)
+    l_b = torch.randn(rows, heads, generator=g, device=dev)
+    out = torch.empty(rows, heads, d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(rows, heads, dtype=torch.float32, device=dev)
+    ms = _time_device(lambda: msa.merge_lse(o_a, l_a, o_b, l_b, out=out, lse=lse), flush)
+    nbytes = rows * heads * (2 * d * 4 + 2 * 4 + d * 2 + 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"rows": rows, "heads": heads, "head_dim": d, "bytes": nbytes, "us": round(ms * 1e3, 2),
+            "GB/s": round(gbs, 1), "roofline": {"bound": "hbm", "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4),
+                                                "peak_source": f"{peak_kind} hbm_gbs"}}
+
+
+def gather_bench(msa, plan, pw, dev, flush, hbm_peak, peak_kind):
+    """The position-order gather of the prefill workload's whole KV context (pool blocks and
+    chunk rows, every KV head) into caller buffers; not part of the step.  Bytes = K and V
+    read and written once, plus the positions written."""
+    import torch
+    st = plan.stats()
+    n, hkv, d = st["kv_tokens"], plan.num_heads_kv, plan.head_dim
+    k = torch.empty(n, hkv, d, dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    pos = torch.empty(n, dtype=torch.int32, device=dev)
+    ms = _time_device(lambda: msa.gather(plan, pw.k_chunk, pw.v_chunk, pw.k_pool, pw.v_pool, out=(k, v, pos)),
+                      flush)
+    nbytes = 2 * (2 * n * hkv * d * 2) + n * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"tokens": n, "bytes": nbytes, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+            "roofline": {"bound": "hbm", "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4),
+                         "peak_source": f"{peak_kind} hbm_gbs"}}
 
 
 def ablation_bench(msa, W, pl, pw, dev, flush, reps: int = 10):

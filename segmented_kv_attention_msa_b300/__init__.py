@@ -374,8 +374,11 @@ def merge_lse(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
     return out, lse
 
 
-def gather(plan: Plan, k_chunk, v_chunk, k_pool, v_pool, stream=None):
-    """KV context of every sequence in canonical (position) order: (K, V, pos)."""
+def gather(plan: Plan, k_chunk, v_chunk, k_pool, v_pool, out=None, stream=None):
+    """KV context of every sequence in canonical (position) order: (K, V, pos).
+
+    `out` = (k, v, pos) writes into caller buffers instead: bf16 [>= n, Hkv, d] twice and
+    int32 [>= n], n = the plan's KV tokens; the first n rows are returned."""
     import torch
     _check_pool(plan, k_pool, v_pool)
     if plan.mode == "prefill" and plan.total_q > 0:
@@ -386,11 +389,23 @@ def gather(plan: Plan, k_chunk, v_chunk, k_pool, v_pool, stream=None):
     dev = k_pool.device
     if plan.dev is None:
         plan.upload(dev, stream)
-    k = torch.empty(max(1, n), plan.num_heads_kv, plan.head_dim, dtype=torch.bfloat16, device=dev)
-    v = torch.empty_like(k)
-    pos = torch.empty(max(1, n), dtype=torch.int32, device=dev)
+    if out is not None:
+        k, v, pos = out
+        for t, name in ((k, "out k"), (v, "out v")):
+            _bf16(t, name)
+            if t.dim() != 3 or t.shape[0] < max(1, n) or tuple(t.shape[1:]) != (plan.num_heads_kv, plan.head_dim):
+                raise ValueError(f"{name}: expected [>= {max(1, n)}, {plan.num_heads_kv}, {plan.head_dim}], "
+                                 f"got {tuple(t.shape)}")
+        if (pos.dtype != torch.int32 or not pos.is_cuda or not pos.is_contiguous() or pos.dim() != 1
+                or pos.shape[0] < max(1, n)):
+            raise ValueError(f"out pos: expected contiguous int32 CUDA [>= {max(1, n)}]")
+    else:
+        k = torch.empty(max(1, n), plan.num_heads_kv, plan.head_dim, dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        pos = torch.empty(max(1, n), dtype=torch.int32, device=dev)
     _check(lib().msa_gather(plan.handle, _dptr(plan.dev), _dptr(k_chunk), _dptr(v_chunk), _dptr(k_pool),
-                            _dptr(v_pool), _dptr(k), _dptr(v), _dptr(pos), k.shape[0], _stream(stream)),
+                            _dptr(v_pool), _dptr(k), _dptr(v), _dptr(pos),
+                            min(k.shape[0], v.shape[0], pos.shape[0]), _stream(stream)),
            "msa_gather")
     return k[:n], v[:n], pos[:n]
 

@@ -95,6 +95,16 @@ def test_gather_bit_exact(idx):
     np.testing.assert_array_equal(pos.cpu().numpy(), p_ref)
     np.testing.assert_array_equal(np64(k), k_ref)
     np.testing.assert_array_equal(np64(v), v_ref)
+    # into caller buffers longer than the context: the same rows, the tail untouched
+    n = k.shape[0]
+    ko = torch.full((n + 5, lay.num_heads_kv, lay.head_dim), 7.0, dtype=torch.bfloat16, device="cuda")
+    vo = torch.full_like(ko, 9.0)
+    po = torch.full((n + 5,), -3, dtype=torch.int32, device="cuda")
+    k2, v2, p2 = msa.gather(plan, wl.k_chunk, wl.v_chunk, wl.k_pool, wl.v_pool, out=(ko, vo, po))
+    torch.cuda.synchronize()
+    assert k2.data_ptr() == ko.data_ptr() and k2.shape[0] == n
+    assert torch.equal(k2, k) and torch.equal(v2, v) and torch.equal(p2, pos)
+    assert torch.all(ko[n:] == 7.0) and torch.all(vo[n:] == 9.0) and torch.all(po[n:] == -3)
 
 
 def test_gather_decode_bit_exact():
