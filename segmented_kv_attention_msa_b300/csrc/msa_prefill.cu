@@ -10,7 +10,8 @@
 //
 // How (one persistent CTA per SM, warp-specialised, 12 warps in 3 warpgroups):
 //  * warp 10 (K producer): TMA loads of the Q tiles (two query heads sharing one KV head,
-//    128 chunk rows each) and of each K tile into a 3-deep ring.  A KV tile is 8 units of
+//    128 chunk rows each; the next work item's Q is prefetched into L2 when an item
+//    starts) and of each K tile into a 3-deep ring.  A KV tile is 8 units of
 //    at most 16 keys, each a paged pool block or a run of chunk rows, loaded as one
 //    16-row box per unit and 64-column slab; pool blocks and chunk rows may share a
 //    tile.  Missing units of a short tile are loaded from an out-of-range row and arrive
