@@ -706,8 +706,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc_fence_after();
       if (wk.nparts == 1) {
         // O leaves TMEM first, every column in flight at once, and the O columns are handed
-        // back before the rows are normalised and stored: the MMA warp may start the next
-        // piece's P.V meanwhile
+        // back before the rows are normalised and stored: this head's issuer may start the
+        // next piece's P.V meanwhile
         uint32_t ov[D];
         tmem_ld_row<D>(tO, ov);
         tc_fence_before();
