@@ -80,21 +80,28 @@ def sources_sha256(name: str) -> str:
 
 
 def kernel_traffic(name: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current code (code_sha256 of the kernel's sources) and applies to this workload;
-    otherwise None."""
-    summ = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
+    """DRAM bytes per launch from a committed ncu summary (profiles/<name>_traffic.txt or
+    profiles/<name>_traffic_<anything>.txt) that was taken on the current code (code_sha256
+    of the kernel's sources) and applies to this workload; otherwise None."""
+    import glob
     try:
-        kv = {}
-        for line in open(summ):
-            if ":" in line:
-                k, v = line.split(":", 1)
-                kv[k.strip()] = v.strip()
-        if kv.get("code_sha256") != sources_sha256(name) or kv.get("applies_to") != workload:
-            return None
-        return float(kv["dram_bytes_per_launch"])
+        current = sources_sha256(name)
     except Exception:
         return None
+    files = [os.path.join(ROOT, "profiles", f"{name}_traffic.txt")]
+    files += sorted(glob.glob(os.path.join(ROOT, "profiles", f"{name}_traffic_*.txt")))
+    for summ in files:
+        try:
+            kv = {}
+            for line in open(summ):
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+            if kv.get("code_sha256") == current and kv.get("applies_to") == workload:
+                return float(kv["dram_bytes_per_launch"])
+        except Exception:
+            continue
+    return None
 
 
 def staging(like, device, sets):

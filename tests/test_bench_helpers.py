@@ -59,6 +59,10 @@ def test_traffic_record_keyed_on_code_and_workload(tmp_path, monkeypatch):
         f"applies_to: wl_a\ncode_sha256: {bench.sources_sha256('k')}\ndram_bytes_per_launch: 1234\n")
     assert bench.kernel_traffic("k", "wl_a") == 1234.0
     assert bench.kernel_traffic("k", "wl_b") is None              # another workload
+    (tmp_path / "profiles" / "k_traffic_wl_b.txt").write_text(    # its own file
+        f"applies_to: wl_b\ncode_sha256: {bench.sources_sha256('k')}\ndram_bytes_per_launch: 99\n")
+    assert bench.kernel_traffic("k", "wl_b") == 99.0
+    assert bench.kernel_traffic("k", "wl_a") == 1234.0
     (csrc / "k.cu").write_text("// a comment\n" + code)
     assert bench.kernel_traffic("k", "wl_a") == 1234.0            # comment-only edit
     (csrc / "p.cpp").write_text("int plan() { return 2; }\n")
@@ -66,3 +70,4 @@ def test_traffic_record_keyed_on_code_and_workload(tmp_path, monkeypatch):
     (csrc / "p.cpp").write_text(plan)
     (csrc / "k.cu").write_text("__global__ void k() { int x = 1; (void)x; }\n")
     assert bench.kernel_traffic("k", "wl_a") is None              # the kernel changed
+    assert bench.kernel_traffic("k", "wl_b") is None
